@@ -1,0 +1,349 @@
+"""Pins for the fp64 oracle: each check is tied to something other than the
+oracle itself -- a hand-worked example from the routing rules (golden/), a
+closed form, brute force on tiny inputs, or a textbook reduction -- so that a
+dropped term, a wrong sign or index, or a transposed operand fails one of them."""
+import itertools
+import json
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+
+def _golden(golden_dir, name):
+    return json.loads((golden_dir / name).read_text())
+
+
+# ---------------------------------------------------------------- router GEMM
+
+def test_router_logits_exact_rational():
+    """logits = x . Wr^T checked against an exact rational dot product."""
+    rng = np.random.default_rng(7)
+    T, E, H = 3, 5, 37
+    x_bits = W.normal_bf16(11, 1, (T, H), 1.0)
+    wr = rng.standard_normal((E, H)).astype(np.float32)
+    got = oracle.router_logits(x_bits, wr)
+    xf = W.bf16_to_f64(x_bits)
+    for t in range(T):
+        for e in range(E):
+            exact = sum(Fraction(float(xf[t, h])) * Fraction(float(wr[e, h])) for h in range(H))
+            assert abs(got[t, e] - float(exact)) <= 1e-13 * max(1.0, abs(float(exact)))
+    # a transposed operand cannot silently pass: shapes are [T,E]
+    assert got.shape == (T, E)
+
+
+def _split_bound_ok(w32):
+    hi, lo = oracle.split_router_weight(w32)
+    w = w32.astype(np.float64)
+    err = np.abs(w - (hi + lo / 256.0))
+    # |W - W_high| <= half a bf16 ulp of W, and |256 r - W_low| <= half a bf16 ulp of 256 r
+    # give |W - (W_high + W_low/256)| <= 2^-16 |W| (normal range).
+    return err <= np.ldexp(np.abs(w), -16), hi, lo
+
+
+def test_router_split_closed_form_bound_sweep():
+    """Closed-form error bound of the two-BF16 split over a sweep of fp32 bit patterns
+    covering every exponent of the normal range and 2^16 mantissas per exponent."""
+    mant = np.arange(0, 1 << 23, 1 << 7, dtype=np.uint32)
+    for exp in range(1, 200, 3):  # keep 256 * r inside the normal range
+        bits = (np.uint32(exp) << np.uint32(23)) | mant
+        for sign in (0, 1):
+            w32 = (bits | np.uint32(sign << 31)).view(np.float32)
+            ok, hi, lo = _split_bound_ok(w32)
+            assert ok.all(), (exp, sign)
+
+
+def test_router_split_is_round_to_nearest_even():
+    """bf16 RNE on hand-picked patterns: ties go to the even mantissa."""
+    def f(bits):
+        return np.array([bits], dtype=np.uint32).view(np.float32)
+    # 1 + 2^-8 is exactly half-way between bf16 1.0 and 1 + 2^-7: rounds to 1.0 (even)
+    assert oracle.bf16_round(f(0x3F808000))[0] == 1.0
+    # 1 + 3*2^-8 is half-way between 1 + 2^-7 (odd) and 1 + 2^-6: rounds up to 1 + 2^-6
+    assert oracle.bf16_round(f(0x3F818000))[0] == 1.0 + 2.0 ** -6
+    # just above the half-way point rounds up
+    assert oracle.bf16_round(f(0x3F808001))[0] == 1.0 + 2.0 ** -7
+    hi, lo = oracle.split_router_weight(f(0x3F808001))
+    assert hi[0] == 1.0 + 2.0 ** -7
+    # residual = (1 + 2^-8 + 2^-23) - (1 + 2^-7) = -2^-8 + 2^-23 ; x256 = -1 + 2^-15 -> bf16 -1
+    assert lo[0] == -1.0
+
+
+def test_router_split_logits_within_bound_of_exact():
+    rng = np.random.default_rng(3)
+    x = W.normal_bf16(5, 1, (8, 512), 1.0)
+    wr = (rng.standard_normal((24, 512)) * 0.02).astype(np.float32)
+    exact = oracle.router_logits(x, wr)
+    hi, lo = oracle.split_router_weight(wr)
+    approx = oracle.router_logits_split(x, hi, lo)
+    bound = (np.abs(W.bf16_to_f64(x)) @ np.ldexp(np.abs(wr.astype(np.float64)), -16).T)
+    assert (np.abs(approx - exact) <= bound + 1e-15).all()
+    rel = np.linalg.norm(approx - exact) / np.linalg.norm(exact)
+    assert rel < 1e-5
+
+
+# ------------------------------------------------------- scoring / top-k / renorm
+
+def test_silu_closed_form(golden_dir):
+    g = _golden(golden_dir, "routing_worked_example.json")["silu"]
+    np.testing.assert_allclose(oracle.silu(np.array(g["g"])), g["silu"], rtol=1e-15, atol=1e-16)
+    # tails: SiLU(g) -> g for large g, -> 0 for very negative g
+    assert oracle.silu(np.array([60.0]))[0] == pytest.approx(60.0, rel=1e-15)
+    assert abs(oracle.silu(np.array([-800.0]))[0]) == 0.0
+
+
+def test_sigmoid_routing_worked_examples(golden_dir):
+    for case in _golden(golden_dir, "routing_worked_example.json")["sigmoid_cases"]:
+        logits = np.array([case["logits"]])
+        r = oracle.route_sigmoid(logits, np.array(case["bias"], dtype=np.float64), case["k"], case["route_scale"])
+        assert r["idx"][0].tolist() == case["idx"], case["note"]
+        np.testing.assert_allclose(r["w"][0], case["w"], rtol=1e-12)
+        assert r["w"][0].sum() / case["route_scale"] == pytest.approx(case["w_unscaled_sum"], abs=1e-12)
+
+
+def test_softmax_routing_worked_example(golden_dir):
+    for case in _golden(golden_dir, "routing_worked_example.json")["softmax_cases"]:
+        r = oracle.route_softmax(np.array([case["logits"]]), case["k"], case["eps"])
+        assert r["idx"][0].tolist() == case["idx"]
+        np.testing.assert_allclose(r["w"][0], case["w"], rtol=1e-12)
+
+
+def _brute_topk(keys, k):
+    """All k-subsets; the top-k set is the one whose every member beats every
+    non-member, where 'beats' is (larger key) or (equal key and lower index)."""
+    E = len(keys)
+
+    def beats(a, b):
+        return keys[a] > keys[b] or (keys[a] == keys[b] and a < b)
+
+    winners = [s for s in itertools.combinations(range(E), k)
+               if all(beats(a, b) for a in s for b in range(E) if b not in s)]
+    assert len(winners) == 1
+    return sorted(winners[0], key=lambda e: (-keys[e], e))
+
+
+def test_topk_brute_force_with_ties():
+    rng = np.random.default_rng(0)
+    for trial in range(300):
+        E = int(rng.integers(2, 8))
+        k = int(rng.integers(1, E + 1))
+        keys = rng.integers(0, 4, size=E).astype(np.float64) / 4.0  # many exact ties
+        idx, margin = oracle.topk_desc(keys[None, :], k)
+        assert idx[0].tolist() == _brute_topk(keys.tolist(), k)
+        srt = sorted(keys, reverse=True)
+        exp_margin = srt[k - 1] - srt[k] if k < E else math.inf
+        assert margin[0] == exp_margin
+
+
+def test_renormalised_weights_sum():
+    rng = np.random.default_rng(1)
+    logits = rng.standard_normal((64, 192)) * 1.3
+    bias = rng.standard_normal(192) * 0.1
+    r1 = oracle.route_sigmoid(logits, bias, 8, 1.0)
+    np.testing.assert_allclose(r1["w"].sum(1), 1.0, atol=1e-12)
+    r2 = oracle.route_sigmoid(logits, bias, 8, 2.826)
+    np.testing.assert_allclose(r2["w"].sum(1), 2.826, atol=1e-12)
+    # the weights are the unbiased sigmoids, not the biased keys
+    s = 1.0 / (1.0 + np.exp(-logits))
+    sel = np.take_along_axis(s, r2["idx"].astype(np.int64), 1)
+    np.testing.assert_allclose(r2["w"], sel / sel.sum(1, keepdims=True) * 2.826, rtol=1e-14)
+
+
+def test_bias_changes_selection_never_weights():
+    rng = np.random.default_rng(2)
+    logits = rng.standard_normal((32, 16))
+    bias = rng.standard_normal(16) * 0.1
+    r = oracle.route_sigmoid(logits, bias, 4, 2.826)
+    # a bias shift that keeps every row's key order keeps the selection; weights identical
+    r_shift = oracle.route_sigmoid(logits, bias + 5.0, 4, 2.826)
+    assert np.array_equal(r["idx"], r_shift["idx"])
+    assert np.array_equal(r["w"], r_shift["w"])
+    # a bias that reorders changes the selection, and the weights are the unbiased
+    # sigmoids of the new selection
+    big = np.zeros(16)
+    big[[3, 5, 7, 9]] = 10.0
+    r_big = oracle.route_sigmoid(logits, big, 4, 2.826)
+    assert (np.sort(r_big["idx"], 1) == np.array([3, 5, 7, 9])).all()
+    s = 1.0 / (1.0 + np.exp(-logits[:, [3, 5, 7, 9]]))
+    np.testing.assert_allclose(np.sort(r_big["w"], 1), np.sort(s / s.sum(1, keepdims=True) * 2.826, 1), rtol=1e-14)
+
+
+def test_softmax_topk_equals_softmax_over_selected():
+    """Closed form: top-k of a softmax renormalised = softmax over the k selected logits."""
+    rng = np.random.default_rng(4)
+    logits = rng.standard_normal((50, 64)) * 2.0
+    r = oracle.route_softmax(logits, 8, 1e-8)
+    sel = np.take_along_axis(logits, r["idx"].astype(np.int64), 1)
+    closed = np.exp(sel - sel.max(1, keepdims=True))
+    closed /= closed.sum(1, keepdims=True)
+    np.testing.assert_allclose(r["w"], closed, rtol=1e-12)
+    np.testing.assert_allclose(r["w"].sum(1), 1.0, atol=1e-13)
+    # selection on the softmax equals selection on the logits (monotone)
+    idx2, _ = oracle.topk_desc(logits, 8)
+    assert np.array_equal(r["idx"], idx2)
+
+
+def test_clamp_degenerate_case():
+    """The clamp only acts when the selected mass is below eps."""
+    sel = np.array([[2e-9, 3e-9], [0.2, 0.3]])
+    w = oracle.renormalize(sel, 1e-8)
+    np.testing.assert_allclose(w[0], [0.2, 0.3], rtol=1e-15)
+    np.testing.assert_allclose(w[1], [0.4, 0.6], rtol=1e-15)
+
+
+def test_near_tie_alternatives():
+    keys = np.array([[0.9, 0.5, 0.5 + 4e-6, 0.1, 0.5 - 3e-6]])
+    mand, cand = oracle.near_tie_alternatives(keys, 2, 1e-5)
+    assert mand[0].tolist() == [True, False, False, False, False]
+    assert cand[0].tolist() == [False, True, True, False, True]
+
+
+# --------------------------------------------------------- histogram / permutation
+
+def test_permutation_brute_force_and_invariants():
+    rng = np.random.default_rng(5)
+    for trial in range(50):
+        T, E = int(rng.integers(1, 20)), int(rng.integers(1, 9))
+        k = int(rng.integers(1, E + 1))
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        counts, offsets = oracle.histogram_offsets(idx, E)
+        perm, inv = oracle.permutation(idx, E)
+        S = T * k
+        assert counts.sum() == S and offsets[-1] == S and offsets[0] == 0
+        assert sorted(perm.tolist()) == list(range(S))          # bijection
+        assert (inv[perm] == np.arange(S)).all() and (perm[inv] == np.arange(S)).all()
+        # brute force: stable sort of slots by (expert, slot)
+        flat = idx.reshape(-1).tolist()
+        expected = sorted(range(S), key=lambda s: (flat[s], s))
+        assert perm.tolist() == expected
+        for e in range(E):
+            seg = perm[offsets[e]:offsets[e + 1]]
+            assert all(flat[s] == e for s in seg) and list(seg) == sorted(seg)
+            assert counts[e] == flat.count(e)
+
+
+# ------------------------------------------------------------- expert FFN / layer
+
+def _dense_swiglu_loops(x, wg, wu, wd):
+    """Independently written dense SwiGLU with explicit index loops:
+    g_i = sum_h Wg[i,h] x_h ; u_i = sum_h Wu[i,h] x_h ; a_i = g_i/(1+e^-g_i) u_i ;
+    y_o = sum_i Wd[o,i] a_i."""
+    T, H = x.shape
+    I = wg.shape[0]
+    y = np.zeros((T, wd.shape[0]))
+    for t in range(T):
+        a = []
+        for i in range(I):
+            g = sum(float(wg[i, h]) * float(x[t, h]) for h in range(H))
+            u = sum(float(wu[i, h]) * float(x[t, h]) for h in range(H))
+            a.append(g / (1.0 + math.exp(-g)) * u)
+        for o in range(wd.shape[0]):
+            y[t, o] = sum(float(wd[o, i]) * a[i] for i in range(I))
+    return y
+
+
+def _tiny_layer_inputs(seed, T, H, E, I, Is):
+    x = W.normal_bf16(seed, 1, (T, H), 1.0)
+    wr = W.normal_f32(seed, 2, (E, H), 0.3)
+    b = W.normal_f32(seed, 3, (E,), 0.1)
+    wg = W.normal_bf16(seed, 4, (E, I, H), 0.3)
+    wu = W.normal_bf16(seed, 5, (E, I, H), 0.3)
+    wd = W.normal_bf16(seed, 6, (E, H, I), 0.3)
+    sg = W.normal_bf16(seed, 7, (Is, H), 0.3)
+    su = W.normal_bf16(seed, 8, (Is, H), 0.3)
+    sd = W.normal_bf16(seed, 9, (H, Is), 0.3)
+    return x, wr, b, wg, wu, wd, sg, su, sd
+
+
+def test_dense_reduction_E1_k1():
+    """E = 1, k = 1: the layer is route_scale x one dense SwiGLU (+ the shared MLP)."""
+    T, H, I, Is = 3, 6, 5, 4
+    x, wr, b, wg, wu, wd, sg, su, sd = _tiny_layer_inputs(21, T, H, 1, I, Is)
+    f = W.bf16_to_f64
+    dense = _dense_swiglu_loops(f(x), f(wg[0]), f(wu[0]), f(wd[0]))
+    shared = _dense_swiglu_loops(f(x), f(sg), f(su), f(sd))
+    r = oracle.layer_forward(x, wr, b, wg, wu, wd, None, None, None, top_k=1, route_scale=2.826)
+    np.testing.assert_allclose(r["out"], 2.826 * dense, rtol=1e-12, atol=1e-12)
+    r = oracle.layer_forward(x, wr, b, wg, wu, wd, sg, su, sd, top_k=1, route_scale=2.826)
+    np.testing.assert_allclose(r["out"], 2.826 * dense + shared, rtol=1e-12, atol=1e-12)
+    r = oracle.layer_forward(x, wr, None, wg, wu, wd, sg, su, sd, top_k=1, score_mode="softmax",
+                             route_scale=1.0, renorm_eps=1e-8)
+    np.testing.assert_allclose(r["out"], dense + shared, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_matches_per_token_brute_force():
+    """Whole layer on a tiny case against per-token loops over the selected experts."""
+    T, H, E, k, I, Is = 5, 6, 4, 2, 3, 5
+    x, wr, b, wg, wu, wd, sg, su, sd = _tiny_layer_inputs(22, T, H, E, I, Is)
+    f = W.bf16_to_f64
+    r = oracle.layer_forward(x, wr, b, wg, wu, wd, sg, su, sd, top_k=k, route_scale=2.826)
+    for t in range(T):
+        logits = [sum(float(f(x)[t, h]) * float(wr[e, h]) for h in range(H)) for e in range(E)]
+        s = [1.0 / (1.0 + math.exp(-v)) for v in logits]
+        keys = [s[e] + float(b[e]) for e in range(E)]
+        chosen = _brute_topk(keys, k)
+        tot = sum(s[e] for e in chosen)
+        out = _dense_swiglu_loops(f(x)[t:t + 1], f(sg), f(su), f(sd))[0]
+        for e in chosen:
+            out = out + (s[e] / tot * 2.826) * _dense_swiglu_loops(f(x)[t:t + 1], f(wg[e]), f(wu[e]), f(wd[e]))[0]
+        np.testing.assert_allclose(r["out"][t], out, rtol=1e-11, atol=1e-12)
+
+
+def test_permutation_equivariance():
+    T, H, E, k, I, Is = 12, 8, 6, 3, 4, 4
+    x, wr, b, wg, wu, wd, sg, su, sd = _tiny_layer_inputs(23, T, H, E, I, Is)
+    r = oracle.layer_forward(x, wr, b, wg, wu, wd, sg, su, sd, top_k=k)
+    p = np.random.default_rng(9).permutation(T)
+    rp = oracle.layer_forward(x[p], wr, b, wg, wu, wd, sg, su, sd, top_k=k)
+    np.testing.assert_allclose(rp["out"], r["out"][p], rtol=1e-13, atol=1e-13)
+    # and a sample of rows equals the same rows of the full batch
+    rows = oracle.layer_rows(x[[2, 7]], wr, b, wg, wu, wd, sg, su, sd, top_k=k)
+    np.testing.assert_allclose(rows["out"], r["out"][[2, 7]], rtol=1e-13, atol=1e-13)
+
+
+def test_combine_brute_force():
+    rng = np.random.default_rng(6)
+    T, k, H = 4, 3, 5
+    y = rng.standard_normal((T * k, H))
+    z = rng.standard_normal((T, H))
+    w = rng.random((T, k))
+    inv = rng.permutation(T * k).astype(np.int32)
+    out = oracle.combine(y, inv, w, z)
+    for t in range(T):
+        for h in range(H):
+            ref = z[t, h] + sum(w[t, j] * y[inv[t * k + j], h] for j in range(k))
+            assert out[t, h] == pytest.approx(ref, rel=1e-14, abs=1e-14)
+
+
+def test_expert_outputs_sorted_rows():
+    """y_sorted[p] is the FFN of expert e applied to token perm[p] // k."""
+    T, H, E, k, I = 7, 6, 3, 2, 4
+    x, wr, b, wg, wu, wd, _, _, _ = _tiny_layer_inputs(24, T, H, E, I, 2)
+    idx = np.array([[0, 2], [1, 0], [2, 1], [0, 1], [2, 0], [1, 2], [0, 2]], dtype=np.int32)
+    counts, offsets = oracle.histogram_offsets(idx, E)
+    perm, inv = oracle.permutation(idx, E)
+    y = oracle.expert_outputs_sorted(x, perm, offsets, k, wg, wu, wd)
+    f = W.bf16_to_f64
+    for p in range(T * k):
+        t, j = divmod(int(perm[p]), k)
+        e = int(idx[t, j])
+        ref = _dense_swiglu_loops(f(x)[t:t + 1], f(wg[e]), f(wu[e]), f(wd[e]))[0]
+        np.testing.assert_allclose(y[p], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_model_facts_match_workloads(golden_dir):
+    facts = _golden(golden_dir, "model_facts.json")
+    d = W.WORKLOADS["decode"]
+    hy3 = facts["hy3"]
+    assert (d.H, d.E, d.top_k, d.I, d.route_scale) == (
+        hy3["hidden_size"], hy3["routed_experts"], hy3["top_k"], hy3["expert_intermediate"],
+        hy3["router_scaling_factor"])
+    img = W.WORKLOADS["image"]
+    hi = facts["hunyuan_image"]
+    assert (img.H, img.E, img.I, img.renorm_eps, img.score_mode) == (
+        hi["hidden_size"], hi["routed_experts"], hi["expert_intermediate"], hi["clamp_min"], hi["score"])
+    assert facts["router_split"]["scale"] == 1.0 / 256.0
