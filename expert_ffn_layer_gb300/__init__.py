@@ -1,0 +1,248 @@
+"""Python binding of libmoe_gb300.so (include/moe.h): argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; PyTorch is used
+here for device memory and streams.  There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+
+Function names follow the C ABI:
+
+    moe_route, moe_permute, moe_expert_ffn, moe_combine, moe_layer_forward,
+    moe_workspace_bytes, moe_ws_init, moe_ws_read_error, moe_check_dims
+
+Tensors are torch tensors on the current CUDA device: bf16 activations and
+weights, fp32 router weight / bias / combine weights, int32 indices, a uint8
+workspace of moe_workspace_bytes(d) bytes (see ``alloc_workspace``).
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT", 6: "MOE_ERR_DEVICE_INDEX"}
+DEVERR_INDEX, DEVERR_TIMEOUT, DEVERR_OFFSETS = 0x1, 0x2, 0x4
+SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
+
+EXPORTS = ("moe_status_string", "moe_check_dims", "moe_workspace_bytes", "moe_ws_init", "moe_ws_read_error",
+           "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)}")
+
+
+class MoeDims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("E", ctypes.c_int), ("I", ctypes.c_int),
+                ("I_shared", ctypes.c_int), ("top_k", ctypes.c_int), ("score_mode", ctypes.c_int),
+                ("route_scale", ctypes.c_float), ("renorm_eps", ctypes.c_float), ("has_shared", ctypes.c_int)]
+
+    def __repr__(self):
+        return "MoeDims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+_lib = None
+
+
+def library_path() -> Path:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not _LIB_PATH.exists():
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with expert_ffn_layer_gb300.build.build() "
+                           "(or __graft_entry__.build()); there is no CPU fallback")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    P, C = ctypes.c_void_p, ctypes.c_size_t
+    D = ctypes.POINTER(MoeDims)
+    st = ctypes.c_int
+    sig = {
+        "moe_status_string": (ctypes.c_char_p, [st]),
+        "moe_check_dims": (st, [D]),
+        "moe_workspace_bytes": (C, [D]),
+        "moe_ws_init": (st, [P, C, P]),
+        "moe_ws_read_error": (st, [P, C, ctypes.c_int, P, ctypes.POINTER(ctypes.c_uint32)]),
+        "moe_route": (st, [D, P, P, P, P, P, P, P, C, P]),
+        "moe_permute": (st, [D, P, P, P, P, P, P, C, P]),
+        "moe_expert_ffn": (st, [D, P, P, P, P, P, P, P, P, P, P, P, P, C, P]),
+        "moe_combine": (st, [D, P, P, P, P, P, P]),
+        "moe_layer_forward": (st, [D, P, P, P, P, P, P, P, P, P, P, P, C, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype, f.argtypes = res, args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().moe_status_string(status).decode()
+
+
+def dims(T: int, H: int, E: int, I: int, top_k: int, I_shared: int | None = None, score_mode: str = "sigmoid",
+         route_scale: float = 2.826, renorm_eps: float = 0.0, has_shared: bool = True) -> MoeDims:
+    mode = {"sigmoid": SCORE_SIGMOID_BIAS, "softmax": SCORE_SOFTMAX}[score_mode]
+    return MoeDims(T, H, E, I, I if I_shared is None else I_shared, top_k, mode, route_scale, renorm_eps,
+                   1 if has_shared else 0)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _check(t, dtype, shape, name):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _call(fn: str, *args):
+    rc = getattr(load(), fn)(*args)
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+def moe_check_dims(d: MoeDims) -> int:
+    return load().moe_check_dims(ctypes.byref(d))
+
+
+def moe_workspace_bytes(d: MoeDims) -> int:
+    n = load().moe_workspace_bytes(ctypes.byref(d))
+    if n == 0:
+        raise MoeError("moe_workspace_bytes", moe_check_dims(d))
+    return n
+
+
+def alloc_workspace(d: MoeDims, device=None) -> torch.Tensor:
+    """A zero-filled uint8 workspace of moe_workspace_bytes(d) bytes."""
+    return torch.zeros(moe_workspace_bytes(d), dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_ws_init(ws: torch.Tensor, stream=None) -> None:
+    _call("moe_ws_init", _ptr(ws), ws.numel(), _stream(stream))
+
+
+def moe_ws_read_error(ws: torch.Tensor, clear: bool = False, stream=None) -> int:
+    bits = ctypes.c_uint32(0)
+    _call("moe_ws_read_error", _ptr(ws), ws.numel(), 1 if clear else 0, _stream(stream), ctypes.byref(bits))
+    return bits.value
+
+
+def moe_route(d: MoeDims, hidden, router_w, expert_bias, topk_idx, topk_w, ws=None, logits_out=None,
+              stream=None) -> None:
+    _check(hidden, torch.bfloat16, (d.T, d.H), "hidden")
+    _check(router_w, torch.float32, (d.E, d.H), "router_w")
+    _check(expert_bias, torch.float32, (d.E,), "expert_bias")
+    _check(topk_idx, torch.int32, (d.T, d.top_k), "topk_idx")
+    _check(topk_w, torch.float32, (d.T, d.top_k), "topk_w")
+    _check(logits_out, torch.float32, (d.T, d.E), "logits_out")
+    _call("moe_route", ctypes.byref(d), _ptr(hidden), _ptr(router_w), _ptr(expert_bias), _ptr(logits_out),
+          _ptr(topk_idx), _ptr(topk_w), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
+
+
+def moe_permute(d: MoeDims, topk_idx, counts, offsets, perm, inv_perm, ws, stream=None) -> None:
+    S = d.T * d.top_k
+    _check(topk_idx, torch.int32, (d.T, d.top_k), "topk_idx")
+    _check(counts, torch.int32, (d.E,), "counts")
+    _check(offsets, torch.int32, (d.E + 1,), "offsets")
+    _check(perm, torch.int32, (S,), "perm")
+    _check(inv_perm, torch.int32, (S,), "inv_perm")
+    _call("moe_permute", ctypes.byref(d), _ptr(topk_idx), _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv_perm),
+          _ptr(ws), ws.numel(), _stream(stream))
+
+
+def moe_expert_ffn(d: MoeDims, hidden, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_sorted,
+                   y_shared, ws, stream=None) -> None:
+    S, Is = d.T * d.top_k, d.I_shared
+    _check(hidden, torch.bfloat16, (d.T, d.H), "hidden")
+    _check(perm, torch.int32, (S,), "perm")
+    _check(offsets, torch.int32, (d.E + 1,), "offsets")
+    _check(w_gate, torch.bfloat16, (d.E, d.I, d.H), "w_gate")
+    _check(w_up, torch.bfloat16, (d.E, d.I, d.H), "w_up")
+    _check(w_down, torch.bfloat16, (d.E, d.H, d.I), "w_down")
+    _check(y_sorted, torch.bfloat16, (S, d.H), "y_sorted")
+    if d.has_shared:
+        _check(ws_gate, torch.bfloat16, (Is, d.H), "ws_gate")
+        _check(ws_up, torch.bfloat16, (Is, d.H), "ws_up")
+        _check(ws_down, torch.bfloat16, (d.H, Is), "ws_down")
+        _check(y_shared, torch.bfloat16, (d.T, d.H), "y_shared")
+    _call("moe_expert_ffn", ctypes.byref(d), _ptr(hidden), _ptr(perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
+          _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(y_sorted), _ptr(y_shared), _ptr(ws),
+          ws.numel(), _stream(stream))
+
+
+def moe_combine(d: MoeDims, y_sorted, y_shared, inv_perm, topk_w, out, stream=None) -> None:
+    S = d.T * d.top_k
+    _check(y_sorted, torch.bfloat16, (S, d.H), "y_sorted")
+    if d.has_shared:
+        _check(y_shared, torch.bfloat16, (d.T, d.H), "y_shared")
+    _check(inv_perm, torch.int32, (S,), "inv_perm")
+    _check(topk_w, torch.float32, (d.T, d.top_k), "topk_w")
+    _check(out, torch.bfloat16, (d.T, d.H), "out")
+    _call("moe_combine", ctypes.byref(d), _ptr(y_sorted), _ptr(y_shared), _ptr(inv_perm), _ptr(topk_w), _ptr(out),
+          _stream(stream))
+
+
+def moe_layer_forward(d: MoeDims, hidden, router_w, expert_bias, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, out,
+                      ws, stream=None) -> None:
+    _check(hidden, torch.bfloat16, (d.T, d.H), "hidden")
+    _check(router_w, torch.float32, (d.E, d.H), "router_w")
+    _check(expert_bias, torch.float32, (d.E,), "expert_bias")
+    _check(w_gate, torch.bfloat16, (d.E, d.I, d.H), "w_gate")
+    _check(w_up, torch.bfloat16, (d.E, d.I, d.H), "w_up")
+    _check(w_down, torch.bfloat16, (d.E, d.H, d.I), "w_down")
+    _check(out, torch.bfloat16, (d.T, d.H), "out")
+    if d.has_shared:
+        _check(ws_gate, torch.bfloat16, (d.I_shared, d.H), "ws_gate")
+        _check(ws_up, torch.bfloat16, (d.I_shared, d.H), "ws_up")
+        _check(ws_down, torch.bfloat16, (d.H, d.I_shared), "ws_down")
+    _call("moe_layer_forward", ctypes.byref(d), _ptr(hidden), _ptr(router_w), _ptr(expert_bias), _ptr(w_gate),
+          _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(out), _ptr(ws), ws.numel(),
+          _stream(stream))
+
+
+class MoELayer:
+    """One MoE FFN layer with device-resident weights and its own workspace:
+    ``layer(hidden)`` runs moe_layer_forward on the current stream."""
+
+    def __init__(self, d: MoeDims, router_w, expert_bias, w_gate, w_up, w_down, ws_gate=None, ws_up=None,
+                 ws_down=None):
+        self.d = d
+        self.router_w, self.expert_bias = router_w, expert_bias
+        self.w_gate, self.w_up, self.w_down = w_gate, w_up, w_down
+        self.ws_gate, self.ws_up, self.ws_down = ws_gate, ws_up, ws_down
+        self.ws = alloc_workspace(d, router_w.device)
+
+    def __call__(self, hidden, out=None, stream=None):
+        if out is None:
+            out = torch.empty((self.d.T, self.d.H), dtype=torch.bfloat16, device=hidden.device)
+        moe_layer_forward(self.d, hidden, self.router_w, self.expert_bias, self.w_gate, self.w_up, self.w_down,
+                          self.ws_gate, self.ws_up, self.ws_down, out, self.ws, stream)
+        return out

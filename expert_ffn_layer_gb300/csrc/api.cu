@@ -1,0 +1,406 @@
+// C ABI (include/moe.h): argument validation, workspace layout, TMA tensor
+// maps, and the launch chain.  Host code only; every step of the layer runs
+// in the kernels of router.cu, permute.cu, expert_gemm.cu and combine.cu.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+
+cudaError_t launch_ex(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                      int cluster_x, void **args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int n = 0;
+  if (pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = (unsigned)cluster_x;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = (unsigned)n;
+  return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+namespace {
+
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *ptr, const uint64_t *dims,
+            const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const uint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void *>(ptr), (const cuuint64_t *)dims,
+                  (const cuuint64_t *)strides_bytes, (const cuuint32_t *)box, (const cuuint32_t *)estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// bf16 matrix [rows][cols] row-major, box {64 cols, box_rows}, 128-byte swizzle
+bool map_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t str[1] = {cols * 2};
+  const uint32_t box[2] = {64, box_rows};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// stacked bf16 [n][rows][cols], box {64, box_rows, 1}, 128-byte swizzle
+bool map_bf16_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t n, uint32_t box_rows) {
+  const uint64_t dims[3] = {cols, rows, n};
+  const uint64_t str[2] = {cols * 2, cols * rows * 2};
+  const uint32_t box[3] = {64, box_rows, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// ------------------------------------------------------------ validation
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+inline bool aligned256(const void *p) { return ((uintptr_t)p & 255u) == 0; }
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct WsLayout {
+  size_t err, topk_idx, topk_w, counts, offsets, perm, inv, y_sorted, y_shared, a_act, a_shared, total;
+};
+
+WsLayout ws_layout(const moe_dims &d) {
+  WsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const size_t T = (size_t)d.T, S = (size_t)d.T * d.top_k, E = (size_t)d.E;
+  const size_t Is = d.has_shared ? (size_t)d.I_shared : 0;
+  L.err = take(256);
+  L.topk_idx = take(S * 4);
+  L.topk_w = take(S * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.perm = take(S * 4);
+  L.inv = take(S * 4);
+  L.y_sorted = take(S * (size_t)d.H * 2);
+  L.y_shared = take(d.has_shared ? T * (size_t)d.H * 2 : 0);
+  L.a_act = take(S * (size_t)d.I * 2);
+  L.a_shared = take(T * Is * 2);
+  L.total = off;
+  return L;
+}
+
+int num_sms() {
+  static thread_local int dev_cached = -1, n = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != dev_cached) {
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    dev_cached = dev;
+  }
+  return n > 0 ? n : 1;
+}
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T>
+inline T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+moe_status check_ws(const moe_dims *d, void *ws, size_t ws_bytes) {
+  if (ws == nullptr || !aligned256(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_layout(*d).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------ stages
+moe_status do_route(const moe_dims &d, const moe_bf16 *hidden, const float *router_w, const float *bias,
+                    float *logits_out, int32_t *topk_idx, float *topk_w, cudaStream_t stream, bool pdl) {
+  RouterParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int Epad = (d.E + 15) & ~15;
+  if (!map_bf16_2d(&p.map_x, hidden, (uint64_t)d.H, (uint64_t)d.T, 128)) return MOE_ERR_CUDA;
+  {
+    const uint64_t dims[2] = {(uint64_t)d.H, (uint64_t)d.E};
+    const uint64_t str[1] = {(uint64_t)d.H * 4};
+    const uint32_t box[2] = {64, (uint32_t)Epad};
+    if (!encode(&p.map_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, router_w, dims, str, box,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MOE_ERR_CUDA;
+  }
+  p.bias = d.score_mode == MOE_SCORE_SIGMOID_BIAS ? bias : nullptr;
+  p.logits_out = logits_out;
+  p.topk_idx = topk_idx;
+  p.topk_w = topk_w;
+  p.T = d.T;
+  p.H = d.H;
+  p.E = d.E;
+  p.Epad = Epad;
+  p.top_k = d.top_k;
+  p.score_mode = d.score_mode;
+  p.route_scale = d.route_scale;
+  p.renorm_eps = d.renorm_eps;
+  p.stages = router_stages(Epad);
+  const int mtiles = (d.T + 127) / 128;
+  const int nslices = d.H / 64;
+  int ks = 8;
+  while (ks > 1 && ((long long)mtiles * ks > num_sms() || nslices % ks != 0)) ks >>= 1;
+  p.kslices_per_cta = nslices / ks;
+  return cuda_status(launch_router(p, ks, mtiles, stream, pdl));
+}
+
+moe_status do_permute(const moe_dims &d, const int32_t *topk_idx, int32_t *counts, int32_t *offsets, int32_t *perm,
+                      int32_t *inv, unsigned *err, cudaStream_t stream, bool pdl) {
+  PermuteParams p;
+  p.topk_idx = topk_idx;
+  p.counts = counts;
+  p.offsets = offsets;
+  p.perm = perm;
+  p.inv = inv;
+  p.err = err;
+  p.S = d.T * d.top_k;
+  p.E = d.E;
+  return cuda_status(launch_permute(p, stream, pdl));
+}
+
+moe_status do_expert_ffn(const moe_dims &d, const moe_bf16 *hidden, const int32_t *perm, const int32_t *offsets,
+                         const moe_bf16 *w_gate, const moe_bf16 *w_up, const moe_bf16 *w_down,
+                         const moe_bf16 *ws_gate, const moe_bf16 *ws_up, const moe_bf16 *ws_down, moe_bf16 *y_sorted,
+                         moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl) {
+  const WsLayout L = ws_layout(d);
+  const int S = d.T * d.top_k;
+  const int Is = d.has_shared ? d.I_shared : 0;
+  moe_bf16 *a_act = at<moe_bf16>(ws, L.a_act);
+  moe_bf16 *a_sh = at<moe_bf16>(ws, L.a_shared);
+  const int bn = gemm_tile_n(d.T);
+  const int nctas = num_sms();
+
+  GemmParams g;
+  std::memset(&g, 0, sizeof(g));
+  g.perm = perm;
+  g.offsets = offsets;
+  g.err = at<unsigned>(ws, L.err);
+  g.T = d.T;
+  g.H = d.H;
+  g.E = d.E;
+  g.I = d.I;
+  g.Is = Is;
+  g.top_k = d.top_k;
+  g.S = S;
+  g.has_shared = d.has_shared;
+
+  // gate/up + SiLU
+  bool ok = map_bf16_3d(&g.map_a0, w_gate, d.H, d.I, d.E, 16) && map_bf16_3d(&g.map_a1, w_up, d.H, d.I, d.E, 16) &&
+            map_bf16_2d(&g.map_b, hidden, d.H, d.T, 1);
+  if (d.has_shared)
+    ok = ok && map_bf16_2d(&g.map_s0, ws_gate, d.H, Is, 16) && map_bf16_2d(&g.map_s1, ws_up, d.H, Is, 16);
+  if (!ok) return MOE_ERR_CUDA;
+  g.out = reinterpret_cast<__nv_bfloat16 *>(a_act);
+  g.out_s = reinterpret_cast<__nv_bfloat16 *>(a_sh);
+  cudaError_t e = launch_expert_gemm(g, kGateUp, bn, nctas, stream, pdl);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // down
+  GemmParams h = g;
+  std::memset(&h.map_a0, 0, sizeof(CUtensorMap) * 6);
+  ok = map_bf16_3d(&h.map_a0, w_down, d.I, d.H, d.E, 128) && map_bf16_2d(&h.map_b, a_act, d.I, S, 16);
+  if (d.has_shared)
+    ok = ok && map_bf16_2d(&h.map_s0, ws_down, Is, d.H, 128) && map_bf16_2d(&h.map_bs, a_sh, Is, d.T, 16);
+  if (!ok) return MOE_ERR_CUDA;
+  h.out = reinterpret_cast<__nv_bfloat16 *>(y_sorted);
+  h.out_s = reinterpret_cast<__nv_bfloat16 *>(y_shared);
+  e = launch_expert_gemm(h, kDown, bn, nctas, stream, true);
+  return cuda_status(e);
+}
+
+moe_status do_combine(const moe_dims &d, const moe_bf16 *y_sorted, const moe_bf16 *y_shared, const int32_t *inv,
+                      const float *topk_w, moe_bf16 *out, cudaStream_t stream, bool pdl) {
+  CombineParams c;
+  c.y_sorted = reinterpret_cast<const __nv_bfloat16 *>(y_sorted);
+  c.y_shared = d.has_shared ? reinterpret_cast<const __nv_bfloat16 *>(y_shared) : nullptr;
+  c.inv = inv;
+  c.topk_w = topk_w;
+  c.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  c.T = d.T;
+  c.H = d.H;
+  c.top_k = d.top_k;
+  c.S = d.T * d.top_k;
+  return cuda_status(launch_combine(c, stream, pdl));
+}
+
+bool ptr_ok(const void *p) { return p != nullptr && aligned16(p); }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API const char *moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null or misaligned pointer, bad size or mode";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape outside the supported set";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace smaller than moe_workspace_bytes()";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA launch or driver call failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel ran out";
+    case MOE_ERR_DEVICE_INDEX: return "MOE_ERR_DEVICE_INDEX: an index seen on the device was out of range";
+  }
+  return "unknown moe_status";
+}
+
+MOE_API moe_status moe_check_dims(const moe_dims *d) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->I <= 0 || d->top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_INVALID_ARG;
+  if (d->has_shared && d->I_shared <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->score_mode != MOE_SCORE_SIGMOID_BIAS && d->score_mode != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(d->route_scale) || !std::isfinite(d->renorm_eps) || d->renorm_eps < 0.0f)
+    return MOE_ERR_INVALID_ARG;
+  if (d->score_mode == MOE_SCORE_SOFTMAX && d->route_scale != 1.0f) return MOE_ERR_INVALID_ARG;
+  if (d->H % 64 != 0 || d->I % 64 != 0 || d->H > 16384 || d->I > 16384) return MOE_ERR_UNSUPPORTED;
+  if (d->has_shared && (d->I_shared % 64 != 0 || d->I_shared > 16384)) return MOE_ERR_UNSUPPORTED;
+  if (d->E > 256 || d->top_k > d->E || d->top_k > 16) return MOE_ERR_UNSUPPORTED;
+  if ((long long)d->T * d->top_k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+MOE_API size_t moe_workspace_bytes(const moe_dims *d) {
+  if (moe_check_dims(d) != MOE_OK) return 0;
+  return ws_layout(*d).total;
+}
+
+MOE_API moe_status moe_ws_init(void *ws, size_t ws_bytes, void *stream) {
+  if (ws == nullptr || !aligned256(ws) || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream));
+}
+
+MOE_API moe_status moe_ws_read_error(void *ws, size_t ws_bytes, int clear, void *stream, uint32_t *bits) {
+  if (ws == nullptr || !aligned256(ws) || ws_bytes < 256 || bits == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  *bits = v;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_route(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
+                             const float *expert_bias, float *logits_out, int32_t *topk_idx, float *topk_w, void *ws,
+                             size_t ws_bytes, void *stream) {
+  (void)ws;
+  (void)ws_bytes;
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;  // empty batch: T-sized buffers may be empty
+  if (!ptr_ok(hidden) || !ptr_ok(router_w) || !ptr_ok(topk_idx) || !ptr_ok(topk_w)) return MOE_ERR_INVALID_ARG;
+  if ((expert_bias != nullptr && !aligned16(expert_bias)) || (logits_out != nullptr && !aligned16(logits_out)))
+    return MOE_ERR_INVALID_ARG;
+  return do_route(*d, hidden, router_w, expert_bias, logits_out, topk_idx, topk_w, (cudaStream_t)stream, true);
+}
+
+MOE_API moe_status moe_permute(const moe_dims *d, const int32_t *topk_idx, int32_t *counts, int32_t *offsets,
+                               int32_t *perm, int32_t *inv_perm, void *ws, size_t ws_bytes, void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (!ptr_ok(counts) || !ptr_ok(offsets)) return MOE_ERR_INVALID_ARG;
+  if (d->T > 0 && (!ptr_ok(topk_idx) || !ptr_ok(perm) || !ptr_ok(inv_perm))) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  if (d->T == 0) {
+    // empty batch: counts and offsets are all zero
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(counts, 0, (size_t)d->E * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, (size_t)(d->E + 1) * 4, s);
+    return cuda_status(e);
+  }
+  return do_permute(*d, topk_idx, counts, offsets, perm, inv_perm, at<unsigned>(ws, ws_layout(*d).err),
+                    (cudaStream_t)stream, true);
+}
+
+MOE_API moe_status moe_expert_ffn(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
+                                  const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                                  const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
+                                  const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws,
+                                  size_t ws_bytes, void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(hidden) || !ptr_ok(perm) || !ptr_ok(offsets) || !ptr_ok(w_gate) || !ptr_ok(w_up) || !ptr_ok(w_down) ||
+      !ptr_ok(y_sorted))
+    return MOE_ERR_INVALID_ARG;
+  if (d->has_shared && (!ptr_ok(ws_gate) || !ptr_ok(ws_up) || !ptr_ok(ws_down) || !ptr_ok(y_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  return do_expert_ffn(*d, hidden, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_sorted, y_shared,
+                       ws, (cudaStream_t)stream, true);
+}
+
+MOE_API moe_status moe_combine(const moe_dims *d, const moe_bf16 *y_sorted, const moe_bf16 *y_shared,
+                               const int32_t *inv_perm, const float *topk_w, moe_bf16 *out, void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(y_sorted) || !ptr_ok(inv_perm) || !ptr_ok(topk_w) || !ptr_ok(out)) return MOE_ERR_INVALID_ARG;
+  if (d->has_shared && !ptr_ok(y_shared)) return MOE_ERR_INVALID_ARG;
+  return do_combine(*d, y_sorted, y_shared, inv_perm, topk_w, out, (cudaStream_t)stream, true);
+}
+
+MOE_API moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
+                                     const float *expert_bias, const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                                     const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
+                                     const moe_bf16 *ws_down, moe_bf16 *out, void *ws, size_t ws_bytes,
+                                     void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(hidden) || !ptr_ok(router_w) || !ptr_ok(w_gate) || !ptr_ok(w_up) || !ptr_ok(w_down) || !ptr_ok(out))
+    return MOE_ERR_INVALID_ARG;
+  if (expert_bias != nullptr && !aligned16(expert_bias)) return MOE_ERR_INVALID_ARG;
+  if (d->has_shared && (!ptr_ok(ws_gate) || !ptr_ok(ws_up) || !ptr_ok(ws_down))) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  const WsLayout L = ws_layout(*d);
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t *idx = at<int32_t>(ws, L.topk_idx);
+  float *w = at<float>(ws, L.topk_w);
+  int32_t *perm = at<int32_t>(ws, L.perm), *inv = at<int32_t>(ws, L.inv);
+  int32_t *offs = at<int32_t>(ws, L.offsets);
+  moe_bf16 *y = at<moe_bf16>(ws, L.y_sorted), *z = at<moe_bf16>(ws, L.y_shared);
+  if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, w, s, true)) != MOE_OK) return st;
+  if ((st = do_permute(*d, idx, at<int32_t>(ws, L.counts), offs, perm, inv, at<unsigned>(ws, L.err), s, true)) !=
+      MOE_OK)
+    return st;
+  if ((st = do_expert_ffn(*d, hidden, perm, offs, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y, z, ws, s,
+                          true)) != MOE_OK)
+    return st;
+  return do_combine(*d, y, z, inv, w, out, s, true);
+}

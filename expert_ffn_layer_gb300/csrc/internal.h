@@ -1,0 +1,79 @@
+// Kernel parameter blocks and launchers shared by the C ABI (api.cu) and the
+// kernels.  Not part of the public interface.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- router
+struct RouterParams {
+  CUtensorMap map_x;  // hidden [T][H] bf16, box {64, 128}, 128-byte swizzle
+  CUtensorMap map_w;  // router_w viewed as {8, E, H/8} fp32 (strides H*4, 32 B), box {8, Epad, 8}
+  const float *bias;  // [E] or nullptr
+  float *logits_out;  // [T][E] or nullptr
+  int32_t *topk_idx;  // [T][k]
+  float *topk_w;      // [T][k]
+  int T, H, E, Epad, top_k, score_mode;
+  float route_scale, renorm_eps;
+  int kslices_per_cta;  // 64-wide K slices handled by one CTA of a cluster
+  int stages;
+};
+constexpr int kRouterThreads = 160;
+size_t router_smem_bytes(int Epad, int stages);
+int router_stages(int Epad);
+cudaError_t launch_router(const RouterParams &p, int ksplit, int mtiles, cudaStream_t stream, bool pdl);
+
+// --------------------------------------------------------------- permute
+struct PermuteParams {
+  const int32_t *topk_idx;  // [S]
+  int32_t *counts;          // [E]
+  int32_t *offsets;         // [E + 1]
+  int32_t *perm;            // [S]
+  int32_t *inv;             // [S]
+  unsigned *err;
+  int S, E;
+};
+cudaError_t launch_permute(const PermuteParams &p, cudaStream_t stream, bool pdl);
+
+// ------------------------------------------------------- grouped expert GEMM
+enum GemmMode { kGateUp = 0, kDown = 1 };
+struct GemmParams {
+  CUtensorMap map_a0;  // gate/up: w_gate {H, I, E} box {64,16,1}; down: w_down {I, H, E} box {64,128,1}
+  CUtensorMap map_a1;  // gate/up: w_up (as map_a0); down: unused
+  CUtensorMap map_s0;  // gate/up: ws_gate {H, Is} box {64,16}; down: ws_down {Is, H} box {64,128}
+  CUtensorMap map_s1;  // gate/up: ws_up; down: unused
+  CUtensorMap map_b;   // gate/up: hidden {H, T} box {64,1} (gather4); down: A_act {I, S} box {64,16}
+  CUtensorMap map_bs;  // down: A_shared {Is, T} box {64,16}; gate/up: unused
+  const int32_t *perm;
+  const int32_t *offsets;
+  __nv_bfloat16 *out;    // gate/up: A_act [S][I]; down: y_sorted [S][H]
+  __nv_bfloat16 *out_s;  // gate/up: A_shared [T][Is]; down: y_shared [T][H]
+  unsigned *err;
+  int T, H, E, I, Is, top_k, S, has_shared;
+};
+constexpr int kGemmThreads = 192;
+int gemm_tile_n(int T);  // tokens per tile (multiple of 16) chosen for a T
+cudaError_t launch_expert_gemm(const GemmParams &p, GemmMode mode, int bn, int num_ctas, cudaStream_t stream,
+                               bool pdl);
+
+// --------------------------------------------------------------- combine
+struct CombineParams {
+  const __nv_bfloat16 *y_sorted;  // [S][H]
+  const __nv_bfloat16 *y_shared;  // [T][H] or nullptr
+  const int32_t *inv;             // [S]
+  const float *topk_w;            // [T][k]
+  __nv_bfloat16 *out;             // [T][H]
+  int T, H, top_k, S;
+};
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream, bool pdl);
+
+// shared launch helper: PDL attribute on, optional cluster dims
+cudaError_t launch_ex(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                      int cluster_x, void **args);
+
+}  // namespace moe

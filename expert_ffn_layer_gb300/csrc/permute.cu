@@ -1,0 +1,154 @@
+// Steps a3-a4: per-expert histogram, offsets and a stable permutation of the
+// flat slots t*k + j into contiguous expert segments.
+//
+// "Hy3 Preview inference optimisation case", section 3 (FusedMoE, routing and
+// index preprocessing): shared-memory block counts reserve one contiguous
+// output range per expert.  The HunyuanImage 3.0 post (Routed Experts) fixes
+// the slot numbering (flattened topk_idx) and the per-expert grouping.
+//
+// One CTA of 32 warps.  Warp w owns a contiguous run of slots.  Pass 1 counts
+// its run per expert in shared memory (warp match + popc); a column scan over
+// the warps and a scan over the experts give every (warp, expert) pair its
+// first output position; pass 2 walks the run again in slot order and ranks
+// equal experts inside a warp with match/popc, so the order inside every
+// segment is ascending slot order -- deterministic, no atomics on positions.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxE = 256;
+constexpr int kUnroll = 8;
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1) permute_kernel(const PermuteParams p) {
+  __shared__ int base[kWarps][kMaxE];
+  __shared__ int offs[kMaxE + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.S, E = p.E;
+  for (int i = threadIdx.x; i < kWarps * kMaxE; i += kThreads) (&base[0][0])[i] = 0;
+
+  pdl_wait();  // topk_idx comes from the router
+  pdl_launch_dependents();
+  __syncthreads();
+
+  const int chunk = (S + kWarps - 1) / kWarps;
+  const int s_begin = min(S, warp * chunk), s_end = min(S, s_begin + chunk);
+  bool bad = false;
+
+  // pass 1: per-warp counts
+  for (int s0 = s_begin; s0 < s_end; s0 += 32 * kUnroll) {
+    int ev[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int s = s0 + 32 * u + lane;
+      ev[u] = s < s_end ? __ldg(p.topk_idx + s) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int s = s0 + 32 * u + lane;
+      const bool valid = s < s_end;
+      int e = ev[u];
+      if (valid && (e < 0 || e >= E)) {
+        bad = true;
+        e = min(max(e, 0), E - 1);
+      }
+      const unsigned active = __ballot_sync(0xffffffffu, valid);
+      if (valid) {
+        const unsigned peers = __match_any_sync(active, e);
+        if (lane == __ffs(peers) - 1) base[warp][e] += __popc(peers);
+      }
+    }
+  }
+  __syncthreads();
+
+  // column scan over warps: base[w][e] <- sum_{w' < w} count[w'][e]; offs[e] <- total
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = base[w][e];
+      base[w][e] = run;
+      run += c;
+    }
+    offs[e] = run;
+  }
+  __syncthreads();
+
+  // exclusive scan over experts (E <= 256 = 32 lanes x 8)
+  if (warp == 0) {
+    int vals[8], local = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane * 8 + j;
+      vals[j] = e < E ? offs[e] : 0;
+      local += vals[j];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int excl = incl - local;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane * 8 + j;
+      if (e < E) {
+        p.counts[e] = vals[j];
+        offs[e] = excl;
+      }
+      excl += vals[j];
+    }
+    if (lane == 31) offs[E] = incl;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += kThreads) p.offsets[e] = offs[e];
+  for (int i = threadIdx.x; i < kWarps * E; i += kThreads) {
+    const int w = i / E, e = i - w * E;
+    base[w][e] += offs[e];
+  }
+  __syncthreads();
+
+  // pass 2: stable scatter in slot order
+  for (int s0 = s_begin; s0 < s_end; s0 += 32 * kUnroll) {
+    int ev[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int s = s0 + 32 * u + lane;
+      ev[u] = s < s_end ? __ldg(p.topk_idx + s) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int s = s0 + 32 * u + lane;
+      const bool valid = s < s_end;
+      const int e = min(max(ev[u], 0), E - 1);
+      const unsigned active = __ballot_sync(0xffffffffu, valid);
+      if (valid) {
+        const unsigned peers = __match_any_sync(active, e);
+        const int leader = __ffs(peers) - 1;
+        int b = 0;
+        if (lane == leader) {
+          b = base[warp][e];
+          base[warp][e] = b + __popc(peers);
+        }
+        b = __shfl_sync(active, b, leader);
+        const int pos = b + __popc(peers & ((1u << lane) - 1u));
+        p.perm[pos] = s;
+        p.inv[s] = pos;
+      }
+    }
+  }
+  if (bad && p.err != nullptr) atomicOr(p.err, MOE_DEVERR_INDEX);
+}
+
+cudaError_t launch_permute(const PermuteParams &p, cudaStream_t stream, bool pdl) {
+  void *args[] = {(void *)&p};
+  return launch_ex((const void *)permute_kernel, dim3(1), dim3(kThreads), 0, stream, pdl, 1, args);
+}
+
+}  // namespace moe

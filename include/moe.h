@@ -1,0 +1,173 @@
+/*
+ * moe.h -- C ABI of a GB300 (sm_103a) forward pass of one Mixture-of-Experts
+ * FFN layer of the Hy3 kind: fp32-accurate router GEMM, sigmoid+bias (or
+ * softmax) top-k routing, per-expert histogram and permutation, grouped
+ * SwiGLU expert GEMMs that read tokens through the route index, an always-on
+ * shared expert, and the top-k weighted combine back to token order.
+ *
+ * Sources (page title, section):
+ *   [hy3]   "hy3 -- tencent/Hy3 GGUF Converter and Inference Engine", Model facts
+ *           (hidden 4096, 192 routed experts top-8 + 1 shared, expert
+ *           intermediate 1536, MoE routing rule, F32 router).
+ *   [case]  "Hy3 Preview inference optimisation case", section 2 Router GEMM
+ *           (W ~ W_high + W_low/256, two BF16 GEMMs, two accumulators, one FFMA
+ *           epilogue) and section 3 FusedMoE (index preprocessing with one
+ *           contiguous range per expert, gate-up GEMM through the route index,
+ *           compact per-expert down GEMM, top-k aggregation at the end, PDL).
+ *   [image] "HunyuanImage 3.0 MoE reading", HunyuanTopKGate easy_topk (softmax,
+ *           top-k, clamp(sum, 1e-8)), Routed Experts (eager loop, weighted sum
+ *           over k, stacked expert weights), Shared MLP.
+ *
+ * Conventions for every entry point
+ *   - bf16 tensors are passed as moe_bf16 (uint16_t bit patterns of bfloat16).
+ *   - Every pointer is a DEVICE pointer owned by the caller, 16-byte aligned
+ *     (the workspace 256-byte aligned).  The library never allocates, frees or
+ *     synchronises; all work is enqueued on `stream` (a cudaStream_t, NULL for
+ *     the legacy default stream) and the call returns once it is enqueued.
+ *   - Weights are nn.Linear [out, in] row-major: w_gate, w_up [E, I, H];
+ *     w_down [E, H, I]; shared ws_gate, ws_up [I_shared, H]; ws_down [H, I_shared].
+ *   - Argument errors are returned before anything is launched:
+ *       MOE_ERR_INVALID_ARG  null / misaligned pointer, negative size, bad mode
+ *       MOE_ERR_UNSUPPORTED  a shape outside the supported set (below)
+ *       MOE_ERR_WORKSPACE    ws_bytes < moe_workspace_bytes(d)
+ *       MOE_ERR_CUDA         a launch or driver call failed
+ *     Anomalies seen on the device (an index outside its range, a bounded wait
+ *     that ran out) are recorded as bits in an error word at the start of the
+ *     workspace and read with moe_ws_read_error().
+ *   - Supported shapes: T >= 0 (T = 0 is a no-op, and T-sized buffers may
+ *     then be NULL; moe_permute still zeroes counts and offsets); H and I (and I_shared when
+ *     has_shared) multiples of 64, H <= 16384, I <= 16384; 1 <= E <= 256;
+ *     1 <= top_k <= min(E, 16); T * top_k < 2^31.
+ *   - The workspace must be zero-filled once after it is allocated (or passed
+ *     to moe_ws_init); the library leaves it reusable.  One workspace must not
+ *     be used by two calls that overlap on the device.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_WORKSPACE = 3,
+  MOE_ERR_CUDA = 4,
+  MOE_ERR_DEVICE_TIMEOUT = 5,
+  MOE_ERR_DEVICE_INDEX = 6
+} moe_status;
+
+typedef enum {
+  MOE_SCORE_SIGMOID_BIAS = 0, /* [hy3] Model facts, MoE routing */
+  MOE_SCORE_SOFTMAX = 1       /* [image] HunyuanTopKGate easy_topk */
+} moe_score_mode;
+
+/* Bits of the device error word (moe_ws_read_error). */
+#define MOE_DEVERR_INDEX 0x1u   /* a routing index or permutation entry out of range (clamped) */
+#define MOE_DEVERR_TIMEOUT 0x2u /* a bounded wait inside a kernel ran out; that kernel gave up */
+#define MOE_DEVERR_OFFSETS 0x4u /* offsets not monotone or offsets[E] != T * top_k; no expert work done */
+
+/* Layer dimensions and routing mode.
+ *   T tokens, H hidden size, E routed experts, I expert intermediate size,
+ *   I_shared shared-expert intermediate size (ignored when has_shared == 0),
+ *   top_k experts per token.
+ *   score_mode MOE_SCORE_SIGMOID_BIAS: s = sigmoid(logits); the top_k is chosen
+ *     on s + expert_bias; weights = s_sel / sum(s_sel) * route_scale ([hy3]:
+ *     route_scale = 2.826).  renorm_eps is not used.
+ *   score_mode MOE_SCORE_SOFTMAX: p = softmax(logits) over the E experts; the
+ *     top_k of p; weights = p_sel / max(sum(p_sel), renorm_eps) ([image]:
+ *     renorm_eps = 1e-8).  route_scale must be 1 and expert_bias is ignored.
+ *   Equal keys go to the lower expert index; topk_idx lists each token's
+ *   experts in descending key order. */
+typedef struct {
+  int T, H, E, I, I_shared, top_k;
+  int score_mode;
+  float route_scale;
+  float renorm_eps;
+  int has_shared;
+} moe_dims;
+
+/* Human-readable name of a status code (static storage). */
+const char *moe_status_string(moe_status s);
+
+/* Validate dims against the supported set; MOE_OK, INVALID_ARG or UNSUPPORTED. */
+moe_status moe_check_dims(const moe_dims *d);
+
+/* Bytes of workspace every entry point below needs for these dims (the fused
+ * layer's need, which covers the others); 0 when the dims are invalid. */
+size_t moe_workspace_bytes(const moe_dims *d);
+
+/* Zero the workspace header (error word and scheduler counters) on `stream`. */
+moe_status moe_ws_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Read (and, with clear != 0, reset) the device error word.  This is the one
+ * call that synchronises `stream`; *bits receives MOE_DEVERR_* flags. */
+moe_status moe_ws_read_error(void *ws, size_t ws_bytes, int clear, void *stream, uint32_t *bits);
+
+/* Steps a1-a2: router GEMM and routing.  [case] section 2; [hy3] MoE routing;
+ * [image] easy_topk.
+ *   hidden      [T, H] bf16 row-major (input)
+ *   router_w    [E, H] fp32 row-major (input); the kernel forms
+ *               W_high = bf16_RNE(W), W_low = bf16_RNE((W - W_high) * 256) on the
+ *               fly, runs two BF16 tensor-core GEMMs into two fp32 accumulators
+ *               and takes logits = acc_lo * (1/256) + acc_hi in one FFMA
+ *   expert_bias [E] fp32 (input, may be NULL = zeros; sigmoid mode only)
+ *   logits_out  [T, E] fp32 (output, may be NULL)
+ *   topk_idx    [T, top_k] int32 (output), topk_w [T, top_k] fp32 (output) */
+moe_status moe_route(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
+                     const float *expert_bias, float *logits_out, int32_t *topk_idx, float *topk_w,
+                     void *ws, size_t ws_bytes, void *stream);
+
+/* Steps a3-a4: per-expert histogram, offsets and permutation.  [case] section 3
+ * (routing and index preprocessing: shared-memory block counts, one contiguous
+ * range per expert); [image] Routed Experts (flattened slot t * top_k + j).
+ *   topk_idx [T, top_k] int32 (input; entries outside [0, E) are clamped and
+ *            flagged with MOE_DEVERR_INDEX)
+ *   counts   [E] int32, offsets [E + 1] int32 (exclusive prefix of counts)
+ *   perm     [T * top_k] int32: perm[p] = flat slot at sorted position p; slots of
+ *            one expert are in ascending slot order (deterministic, stable)
+ *   inv_perm [T * top_k] int32: inv_perm[slot] = p */
+moe_status moe_permute(const moe_dims *d, const int32_t *topk_idx, int32_t *counts, int32_t *offsets,
+                       int32_t *perm, int32_t *inv_perm, void *ws, size_t ws_bytes, void *stream);
+
+/* Steps a5-a8: grouped gate/up GEMM reading hidden rows through perm (no gather
+ * copy), SiLU(gate) * up, grouped down GEMM, and the shared expert.  [case]
+ * section 3; [image] Routed Experts and Shared MLP.
+ *   hidden   [T, H] bf16; perm [T * top_k], offsets [E + 1] as moe_permute writes them
+ *   w_gate, w_up [E, I, H] bf16; w_down [E, H, I] bf16
+ *   ws_gate, ws_up [I_shared, H]; ws_down [H, I_shared] bf16 (NULL when !has_shared)
+ *   y_sorted [T * top_k, H] bf16 (output): y_sorted[p] = FFN_e(hidden[perm[p] / top_k])
+ *            for p in expert e's range
+ *   y_shared [T, H] bf16 (output, NULL when !has_shared): shared FFN of every token */
+moe_status moe_expert_ffn(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
+                          const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                          const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
+                          const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws,
+                          size_t ws_bytes, void *stream);
+
+/* Step a9: out[t] = sum_j topk_w[t, j] * y_sorted[inv_perm[t * top_k + j]] + y_shared[t]
+ * (fp32 sum in j order, one bf16 rounding).  [case] section 3 (top-k weighted
+ * aggregation at the end); [image] Routed Experts (weighted sum over k) and
+ * Shared MLP (added).  y_shared may be NULL when !has_shared. */
+moe_status moe_combine(const moe_dims *d, const moe_bf16 *y_sorted, const moe_bf16 *y_shared,
+                       const int32_t *inv_perm, const float *topk_w, moe_bf16 *out, void *stream);
+
+/* The whole layer (a1-a9) chained on `stream` with programmatic dependent
+ * launch; every intermediate lives in `ws`.  Arguments as above; out [T, H] bf16. */
+moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
+                             const float *expert_bias, const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                             const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
+                             const moe_bf16 *ws_down, moe_bf16 *out, void *ws, size_t ws_bytes,
+                             void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

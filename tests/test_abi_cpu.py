@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/moe.h declares, and validates arguments before it
+launches anything (invalid calls return an error without touching CUDA)."""
+import ctypes
+import re
+
+import pytest
+
+import __graft_entry__
+import expert_ffn_layer_gb300 as moe
+
+ROOT = __graft_entry__.ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return moe.load()
+
+
+def _declared_functions():
+    text = (ROOT / "include" / "moe.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 10
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(moe.EXPORTS) == declared
+
+
+def test_status_strings(lib):
+    for code, name in moe.STATUS.items():
+        assert moe.status_string(code).startswith(name)
+
+
+def _hy3(T=8):
+    return moe.dims(T, 4096, 192, 1536, 8)
+
+
+def test_check_dims(lib):
+    assert moe.moe_check_dims(_hy3()) == 0
+    assert moe.moe_check_dims(moe.dims(0, 4096, 192, 1536, 8)) == 0          # empty batch is valid
+    assert moe.moe_check_dims(moe.dims(8, 4000, 192, 1536, 8)) == 2          # H % 64
+    assert moe.moe_check_dims(moe.dims(8, 4096, 192, 1500, 8)) == 2          # I % 64
+    assert moe.moe_check_dims(moe.dims(8, 4096, 300, 1536, 8)) == 2          # E > 256
+    assert moe.moe_check_dims(moe.dims(8, 4096, 8, 1536, 9)) == 2           # k > E
+    assert moe.moe_check_dims(moe.dims(8, 4096, 64, 1536, 17)) == 2         # k > 16
+    assert moe.moe_check_dims(moe.dims(-1, 4096, 64, 1536, 8)) == 1
+    assert moe.moe_check_dims(moe.dims(8, 4096, 64, 1536, 0)) == 1
+    assert moe.moe_check_dims(moe.dims(8, 4096, 64, 1536, 8, score_mode="softmax", route_scale=2.0)) == 1
+    assert moe.moe_check_dims(moe.dims(8, 4096, 64, 1536, 8, renorm_eps=-1.0)) == 1
+    assert moe.moe_check_dims(moe.dims(8, 4096, 64, 1536, 8, I_shared=100)) == 2
+    assert moe.moe_check_dims(moe.dims(8, 4096, 64, 1536, 8, I_shared=100, has_shared=False)) == 0
+
+
+def test_workspace_bytes(lib):
+    d = _hy3(4096)
+    n = moe.moe_workspace_bytes(d)
+    S = 4096 * 8
+    # dominated by y_sorted [S,H], y_shared [T,H], A_act [S,I], A_shared [T,I] (bf16)
+    core = 2 * (S * 4096 + 4096 * 4096 + S * 1536 + 4096 * 1536)
+    assert core <= n <= core + 1 << 20
+    assert n % 256 == 0
+    assert moe.moe_workspace_bytes(_hy3(8)) < n
+    assert lib.moe_workspace_bytes(ctypes.byref(moe.dims(8, 4000, 192, 1536, 8))) == 0
+
+
+def test_invalid_arguments_are_rejected_before_launch(lib):
+    d = _hy3()
+    byref = ctypes.byref
+    # null pointers
+    assert lib.moe_route(byref(d), None, None, None, None, None, None, None, 0, None) == 1
+    assert lib.moe_permute(byref(d), None, None, None, None, None, None, 0, None) == 1
+    assert lib.moe_expert_ffn(byref(d), *([None] * 12), 0, None) == 1
+    assert lib.moe_combine(byref(d), None, None, None, None, None, None) == 1
+    assert lib.moe_layer_forward(byref(d), *([None] * 11), 0, None) == 1
+    # misaligned pointer (never dereferenced: validation fails first)
+    bad = 0x1003
+    assert lib.moe_combine(byref(d), bad, bad, bad, bad, bad, None) == 1
+    # a short workspace is reported as such (pointers aligned, never dereferenced)
+    good = 0x100000
+    args = [good] * 10  # hidden, router_w, bias, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, out
+    assert lib.moe_layer_forward(byref(d), *args, good, 16, None) == 3
+    # unsupported shapes win over pointer checks
+    assert lib.moe_route(byref(moe.dims(8, 4000, 192, 1536, 8)), good, good, None, None, good, good, None, 0,
+                         None) == 2
+    assert lib.moe_ws_init(None, 0, None) == 1
+    bits = ctypes.c_uint32()
+    assert lib.moe_ws_read_error(None, 0, 0, None, byref(bits)) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import importlib
+
+    monkeypatch.setattr(moe, "_lib", None)
+    monkeypatch.setattr(moe, "_LIB_PATH", tmp_path / "missing.so")
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        moe.load()
+    importlib.reload(moe)
