@@ -6,7 +6,8 @@ missing or a call fails, an exception is raised.
 
 Function names follow the C ABI:
 
-    moe_route, moe_permute, moe_expert_ffn, moe_combine, moe_layer_forward,
+    moe_route, moe_permute, moe_expert_ffn (= moe_expert_gate_up + moe_expert_down),
+    moe_combine, moe_layer_forward,
     moe_workspace_bytes, moe_ws_init, moe_ws_read_error, moe_check_dims
 
 Tensors are torch tensors on the current CUDA device: bf16 activations and
@@ -29,7 +30,8 @@ DEVERR_INDEX, DEVERR_TIMEOUT, DEVERR_OFFSETS = 0x1, 0x2, 0x4
 SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
 
 EXPORTS = ("moe_status_string", "moe_check_dims", "moe_workspace_bytes", "moe_ws_init", "moe_ws_read_error",
-           "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward")
+           "moe_route", "moe_permute", "moe_expert_ffn", "moe_expert_gate_up", "moe_expert_down", "moe_combine",
+           "moe_layer_forward")
 
 
 class MoeError(RuntimeError):
@@ -75,6 +77,8 @@ def load() -> ctypes.CDLL:
         "moe_route": (st, [D, P, P, P, P, P, P, P, C, P]),
         "moe_permute": (st, [D, P, P, P, P, P, P, C, P]),
         "moe_expert_ffn": (st, [D, P, P, P, P, P, P, P, P, P, P, P, P, C, P]),
+        "moe_expert_gate_up": (st, [D, P, P, P, P, P, P, P, P, C, P]),
+        "moe_expert_down": (st, [D, P, P, P, P, P, P, C, P]),
         "moe_combine": (st, [D, P, P, P, P, P, P]),
         "moe_layer_forward": (st, [D, P, P, P, P, P, P, P, P, P, P, P, C, P]),
     }
@@ -196,6 +200,16 @@ def moe_expert_ffn(d: MoeDims, hidden, perm, offsets, w_gate, w_up, w_down, ws_g
     _call("moe_expert_ffn", ctypes.byref(d), _ptr(hidden), _ptr(perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
           _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(y_sorted), _ptr(y_shared), _ptr(ws),
           ws.numel(), _stream(stream))
+
+
+def moe_expert_gate_up(d: MoeDims, hidden, perm, offsets, w_gate, w_up, ws_gate, ws_up, ws, stream=None) -> None:
+    _call("moe_expert_gate_up", ctypes.byref(d), _ptr(hidden), _ptr(perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
+          _ptr(ws_gate), _ptr(ws_up), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def moe_expert_down(d: MoeDims, offsets, w_down, ws_down, y_sorted, y_shared, ws, stream=None) -> None:
+    _call("moe_expert_down", ctypes.byref(d), _ptr(offsets), _ptr(w_down), _ptr(ws_down), _ptr(y_sorted),
+          _ptr(y_shared), _ptr(ws), ws.numel(), _stream(stream))
 
 
 def moe_combine(d: MoeDims, y_sorted, y_shared, inv_perm, topk_w, out, stream=None) -> None:

@@ -144,9 +144,11 @@ moe_status check_ws(const moe_dims *d, void *ws, size_t ws_bytes) {
 
 // ------------------------------------------------------------ stages
 moe_status do_route(const moe_dims &d, const moe_bf16 *hidden, const float *router_w, const float *bias,
-                    float *logits_out, int32_t *topk_idx, float *topk_w, cudaStream_t stream, bool pdl) {
+                    float *logits_out, int32_t *topk_idx, float *topk_w, unsigned *err, cudaStream_t stream,
+                    bool pdl) {
   RouterParams p;
   std::memset(&p, 0, sizeof(p));
+  p.err = err;
   const int Epad = (d.E + 15) & ~15;
   if (!map_bf16_2d(&p.map_x, hidden, (uint64_t)d.H, (uint64_t)d.T, 128)) return MOE_ERR_CUDA;
   {
@@ -192,18 +194,8 @@ moe_status do_permute(const moe_dims &d, const int32_t *topk_idx, int32_t *count
   return cuda_status(launch_permute(p, stream, pdl));
 }
 
-moe_status do_expert_ffn(const moe_dims &d, const moe_bf16 *hidden, const int32_t *perm, const int32_t *offsets,
-                         const moe_bf16 *w_gate, const moe_bf16 *w_up, const moe_bf16 *w_down,
-                         const moe_bf16 *ws_gate, const moe_bf16 *ws_up, const moe_bf16 *ws_down, moe_bf16 *y_sorted,
-                         moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl) {
+GemmParams gemm_common(const moe_dims &d, const int32_t *perm, const int32_t *offsets, void *ws) {
   const WsLayout L = ws_layout(d);
-  const int S = d.T * d.top_k;
-  const int Is = d.has_shared ? d.I_shared : 0;
-  moe_bf16 *a_act = at<moe_bf16>(ws, L.a_act);
-  moe_bf16 *a_sh = at<moe_bf16>(ws, L.a_shared);
-  const int bn = gemm_tile_n(d.T);
-  const int nctas = num_sms();
-
   GemmParams g;
   std::memset(&g, 0, sizeof(g));
   g.perm = perm;
@@ -213,33 +205,52 @@ moe_status do_expert_ffn(const moe_dims &d, const moe_bf16 *hidden, const int32_
   g.H = d.H;
   g.E = d.E;
   g.I = d.I;
-  g.Is = Is;
+  g.Is = d.has_shared ? d.I_shared : 0;
   g.top_k = d.top_k;
-  g.S = S;
+  g.S = d.T * d.top_k;
   g.has_shared = d.has_shared;
+  return g;
+}
 
-  // gate/up + SiLU
+// a5-a6: gate/up GEMM through the route index + SiLU(gate) * up -> activations in ws
+moe_status do_gate_up(const moe_dims &d, const moe_bf16 *hidden, const int32_t *perm, const int32_t *offsets,
+                      const moe_bf16 *w_gate, const moe_bf16 *w_up, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
+                      void *ws, cudaStream_t stream, bool pdl) {
+  const WsLayout L = ws_layout(d);
+  GemmParams g = gemm_common(d, perm, offsets, ws);
   bool ok = map_bf16_3d(&g.map_a0, w_gate, d.H, d.I, d.E, 16) && map_bf16_3d(&g.map_a1, w_up, d.H, d.I, d.E, 16) &&
             map_bf16_2d(&g.map_b, hidden, d.H, d.T, 1);
   if (d.has_shared)
-    ok = ok && map_bf16_2d(&g.map_s0, ws_gate, d.H, Is, 16) && map_bf16_2d(&g.map_s1, ws_up, d.H, Is, 16);
+    ok = ok && map_bf16_2d(&g.map_s0, ws_gate, d.H, g.Is, 16) && map_bf16_2d(&g.map_s1, ws_up, d.H, g.Is, 16);
   if (!ok) return MOE_ERR_CUDA;
-  g.out = reinterpret_cast<__nv_bfloat16 *>(a_act);
-  g.out_s = reinterpret_cast<__nv_bfloat16 *>(a_sh);
-  cudaError_t e = launch_expert_gemm(g, kGateUp, bn, nctas, stream, pdl);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  g.out = at<__nv_bfloat16>(ws, L.a_act);
+  g.out_s = at<__nv_bfloat16>(ws, L.a_shared);
+  return cuda_status(launch_expert_gemm(g, kGateUp, gemm_tile_n(d.T), num_sms(), stream, pdl));
+}
 
-  // down
-  GemmParams h = g;
-  std::memset(&h.map_a0, 0, sizeof(CUtensorMap) * 6);
-  ok = map_bf16_3d(&h.map_a0, w_down, d.I, d.H, d.E, 128) && map_bf16_2d(&h.map_b, a_act, d.I, S, 16);
+// a7-a8: down GEMM over the activations in ws -> y_sorted, y_shared
+moe_status do_down(const moe_dims &d, const int32_t *offsets, const moe_bf16 *w_down, const moe_bf16 *ws_down,
+                   moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl) {
+  const WsLayout L = ws_layout(d);
+  GemmParams h = gemm_common(d, nullptr, offsets, ws);
+  bool ok = map_bf16_3d(&h.map_a0, w_down, d.I, d.H, d.E, 128) &&
+            map_bf16_2d(&h.map_b, at<moe_bf16>(ws, L.a_act), d.I, h.S, 16);
   if (d.has_shared)
-    ok = ok && map_bf16_2d(&h.map_s0, ws_down, Is, d.H, 128) && map_bf16_2d(&h.map_bs, a_sh, Is, d.T, 16);
+    ok = ok && map_bf16_2d(&h.map_s0, ws_down, h.Is, d.H, 128) &&
+         map_bf16_2d(&h.map_bs, at<moe_bf16>(ws, L.a_shared), h.Is, d.T, 16);
   if (!ok) return MOE_ERR_CUDA;
   h.out = reinterpret_cast<__nv_bfloat16 *>(y_sorted);
   h.out_s = reinterpret_cast<__nv_bfloat16 *>(y_shared);
-  e = launch_expert_gemm(h, kDown, bn, nctas, stream, true);
-  return cuda_status(e);
+  return cuda_status(launch_expert_gemm(h, kDown, gemm_tile_n(d.T), num_sms(), stream, pdl));
+}
+
+moe_status do_expert_ffn(const moe_dims &d, const moe_bf16 *hidden, const int32_t *perm, const int32_t *offsets,
+                         const moe_bf16 *w_gate, const moe_bf16 *w_up, const moe_bf16 *w_down,
+                         const moe_bf16 *ws_gate, const moe_bf16 *ws_up, const moe_bf16 *ws_down, moe_bf16 *y_sorted,
+                         moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl) {
+  moe_status st = do_gate_up(d, hidden, perm, offsets, w_gate, w_up, ws_gate, ws_up, ws, stream, pdl);
+  if (st != MOE_OK) return st;
+  return do_down(d, offsets, w_down, ws_down, y_sorted, y_shared, ws, stream, true);
 }
 
 moe_status do_combine(const moe_dims &d, const moe_bf16 *y_sorted, const moe_bf16 *y_shared, const int32_t *inv,
@@ -318,15 +329,19 @@ MOE_API moe_status moe_ws_read_error(void *ws, size_t ws_bytes, int clear, void 
 MOE_API moe_status moe_route(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
                              const float *expert_bias, float *logits_out, int32_t *topk_idx, float *topk_w, void *ws,
                              size_t ws_bytes, void *stream) {
-  (void)ws;
-  (void)ws_bytes;
   moe_status st = moe_check_dims(d);
   if (st != MOE_OK) return st;
   if (d->T == 0) return MOE_OK;  // empty batch: T-sized buffers may be empty
   if (!ptr_ok(hidden) || !ptr_ok(router_w) || !ptr_ok(topk_idx) || !ptr_ok(topk_w)) return MOE_ERR_INVALID_ARG;
   if ((expert_bias != nullptr && !aligned16(expert_bias)) || (logits_out != nullptr && !aligned16(logits_out)))
     return MOE_ERR_INVALID_ARG;
-  return do_route(*d, hidden, router_w, expert_bias, logits_out, topk_idx, topk_w, (cudaStream_t)stream, true);
+  // the workspace is optional here: when given, device-side anomalies are recorded in its error word
+  unsigned *err = nullptr;
+  if (ws != nullptr) {
+    if (!aligned256(ws) || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
+    err = at<unsigned>(ws, 0);
+  }
+  return do_route(*d, hidden, router_w, expert_bias, logits_out, topk_idx, topk_w, err, (cudaStream_t)stream, true);
 }
 
 MOE_API moe_status moe_permute(const moe_dims *d, const int32_t *topk_idx, int32_t *counts, int32_t *offsets,
@@ -365,6 +380,32 @@ MOE_API moe_status moe_expert_ffn(const moe_dims *d, const moe_bf16 *hidden, con
                        ws, (cudaStream_t)stream, true);
 }
 
+MOE_API moe_status moe_expert_gate_up(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
+                                      const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                                      const moe_bf16 *ws_gate, const moe_bf16 *ws_up, void *ws, size_t ws_bytes,
+                                      void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(hidden) || !ptr_ok(perm) || !ptr_ok(offsets) || !ptr_ok(w_gate) || !ptr_ok(w_up))
+    return MOE_ERR_INVALID_ARG;
+  if (d->has_shared && (!ptr_ok(ws_gate) || !ptr_ok(ws_up))) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  return do_gate_up(*d, hidden, perm, offsets, w_gate, w_up, ws_gate, ws_up, ws, (cudaStream_t)stream, true);
+}
+
+MOE_API moe_status moe_expert_down(const moe_dims *d, const int32_t *offsets, const moe_bf16 *w_down,
+                                   const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws,
+                                   size_t ws_bytes, void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(offsets) || !ptr_ok(w_down) || !ptr_ok(y_sorted)) return MOE_ERR_INVALID_ARG;
+  if (d->has_shared && (!ptr_ok(ws_down) || !ptr_ok(y_shared))) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  return do_down(*d, offsets, w_down, ws_down, y_sorted, y_shared, ws, (cudaStream_t)stream, true);
+}
+
 MOE_API moe_status moe_combine(const moe_dims *d, const moe_bf16 *y_sorted, const moe_bf16 *y_shared,
                                const int32_t *inv_perm, const float *topk_w, moe_bf16 *out, void *stream) {
   moe_status st = moe_check_dims(d);
@@ -395,7 +436,9 @@ MOE_API moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, 
   int32_t *perm = at<int32_t>(ws, L.perm), *inv = at<int32_t>(ws, L.inv);
   int32_t *offs = at<int32_t>(ws, L.offsets);
   moe_bf16 *y = at<moe_bf16>(ws, L.y_sorted), *z = at<moe_bf16>(ws, L.y_shared);
-  if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, w, s, true)) != MOE_OK) return st;
+  if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, w, at<unsigned>(ws, L.err), s, true)) !=
+      MOE_OK)
+    return st;
   if ((st = do_permute(*d, idx, at<int32_t>(ws, L.counts), offs, perm, inv, at<unsigned>(ws, L.err), s, true)) !=
       MOE_OK)
     return st;

@@ -13,9 +13,10 @@ namespace moe {
 // ---------------------------------------------------------------- router
 struct RouterParams {
   CUtensorMap map_x;  // hidden [T][H] bf16, box {64, 128}, 128-byte swizzle
-  CUtensorMap map_w;  // router_w viewed as {8, E, H/8} fp32 (strides H*4, 32 B), box {8, Epad, 8}
+  CUtensorMap map_w;  // router_w [E][H] fp32, box {64, Epad}, no swizzle (rows >= E read as zero)
   const float *bias;  // [E] or nullptr
   float *logits_out;  // [T][E] or nullptr
+  unsigned *err;      // workspace error word or nullptr
   int32_t *topk_idx;  // [T][k]
   float *topk_w;      // [T][k]
   int T, H, E, Epad, top_k, score_mode;
@@ -23,7 +24,7 @@ struct RouterParams {
   int kslices_per_cta;  // 64-wide K slices handled by one CTA of a cluster
   int stages;
 };
-constexpr int kRouterThreads = 160;
+constexpr int kRouterThreads = 192;  // warps 0-3 convert + epilogue, 4 MMA, 5 TMA
 size_t router_smem_bytes(int Epad, int stages);
 int router_stages(int Epad);
 cudaError_t launch_router(const RouterParams &p, int ksplit, int mtiles, cudaStream_t stream, bool pdl);

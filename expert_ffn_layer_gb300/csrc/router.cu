@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  unsigned *err = nullptr;  // the router has no workspace error word; timeouts abort quietly
+  unsigned *err = p.err;
 
   pdl_wait();  // hidden may come from the previous kernel of a chain
   pdl_launch_dependents();

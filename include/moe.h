@@ -121,6 +121,8 @@ moe_status moe_ws_read_error(void *ws, size_t ws_bytes, int clear, void *stream,
  *   expert_bias [E] fp32 (input, may be NULL = zeros; sigmoid mode only)
  *   logits_out  [T, E] fp32 (output, may be NULL)
  *   topk_idx    [T, top_k] int32 (output), topk_w [T, top_k] fp32 (output) */
+/* ws may be NULL (this step needs no scratch); when given (>= 256 bytes, 256-byte
+ * aligned), device-side anomalies are recorded in its error word. */
 moe_status moe_route(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
                      const float *expert_bias, float *logits_out, int32_t *topk_idx, float *topk_w,
                      void *ws, size_t ws_bytes, void *stream);
@@ -151,6 +153,20 @@ moe_status moe_expert_ffn(const moe_dims *d, const moe_bf16 *hidden, const int32
                           const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
                           const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws,
                           size_t ws_bytes, void *stream);
+
+/* The two kernels of moe_expert_ffn as separate calls (same kernels, same
+ * results): the gate/up half (a5-a6) writes the bf16 activation
+ * SiLU(gate) * up of every routed slot and every token's shared-expert
+ * activation into the workspace; the down half (a7-a8) reads them from the
+ * same workspace and writes y_sorted / y_shared.  Call them in this order on
+ * one stream with one workspace; arguments as for moe_expert_ffn. */
+moe_status moe_expert_gate_up(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
+                              const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                              const moe_bf16 *ws_gate, const moe_bf16 *ws_up, void *ws, size_t ws_bytes,
+                              void *stream);
+moe_status moe_expert_down(const moe_dims *d, const int32_t *offsets, const moe_bf16 *w_down,
+                           const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws,
+                           size_t ws_bytes, void *stream);
 
 /* Step a9: out[t] = sum_j topk_w[t, j] * y_sorted[inv_perm[t * top_k + j]] + y_shared[t]
  * (fp32 sum in j order, one bf16 rounding).  [case] section 3 (top-k weighted
