@@ -1,0 +1,519 @@
+#!/usr/bin/env python3
+"""Throughput of one Hy3-style MoE FFN layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one whole layer forward (router GEMM + top-k, permutation, grouped
+gate/up GEMM + SiLU, grouped down GEMM with the shared expert, combine) through
+the C ABI on one batch of seeded synthetic input of the pages' shapes, with
+weights resident in HBM.  The headline workload is the Hy3 decode batch
+(T = 8 tokens, H = 4096, 192 routed experts top-8 + 1 shared, I = 1536); the
+Hy3 prefill chunk (T = 4096) is measured too and reported in "prefill".
+
+L2 is flushed (a 256 MiB write) between timed steps; each step is timed with
+CUDA events on the launching stream.  Under torchrun each rank runs its own
+replica on its own tokens (weak scaling, no collective on the data path) and
+the slowest rank's time is used.
+
+--impl reference times the fp64 oracle (oracle/) on the host cores on the same
+workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "MoE-layer tokens/s at Hy3 shape (T=8, T=4096); % of HBM or BF16 tensor roofline"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash() -> str:
+    """Hash of the CUDA sources: stored ncu counters are used only for the same kernels."""
+    h = hashlib.sha256()
+    for f in sorted((ROOT / "expert_ffn_layer_gb300" / "csrc").glob("*")):
+        h.update(f.name.encode())
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    """dram bytes per launch from a committed ncu summary, if it matches these sources."""
+    p = ROOT / "profiles" / f"dram_traffic_{workload}.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text())
+    if d.get("source_hash") != source_hash():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else float(k["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = [r.split(", ") for r in Path(self.file.name).read_text().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def stage_work(w, n_active: int):
+    """Algorithmic bytes and FLOPs of each kernel of one layer forward."""
+    T, H, E, k, I = w.T, w.H, w.E, w.top_k, w.I
+    S = T * k
+    Is = w.I_shared if w.has_shared else 0
+    Ts = T if w.has_shared else 0
+    ns = 1 if w.has_shared else 0
+    return {
+        "route": {"bytes": E * H * 4 + T * H * 2 + S * 8 + E * 4, "flops": 2 * 2 * T * H * E},
+        "permute": {"bytes": S * 4 * 3 + (2 * E + 1) * 4, "flops": 0},
+        "gate_up": {"bytes": (n_active * 2 * I + ns * 2 * Is) * H * 2 + (S + Ts) * H * 2 + (S * I + Ts * Is) * 2,
+                    "flops": 4 * (S * H * I + Ts * H * Is)},
+        "down": {"bytes": (n_active * I + ns * Is) * H * 2 + (S * I + Ts * Is) * 2 + (S + Ts) * H * 2,
+                 "flops": 2 * (S * H * I + Ts * H * Is)},
+        "combine": {"bytes": S * H * 2 + Ts * H * 2 + T * H * 2 + S * 8, "flops": 2 * S * H},
+    }
+
+
+def roofline_for(stage: str, work: dict, ms: float, pk: dict, pk_kind: str, workload: str, bound: str | None = None):
+    b, f = work[stage]["bytes"], work[stage]["flops"]
+    t_mem = b / (pk["hbm_gbs"] * 1e9)
+    t_tc = f / (pk["bf16_tflops"] * 1e12) if f else 0.0
+    if bound is None:
+        bound = "tensor" if t_tc > t_mem else "hbm"
+    sec = ms * 1e-3
+    if bound == "hbm":
+        ach, peak, unit = b / sec / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        ach, peak, unit = f / sec / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    return {"kernel": stage, "bound": bound, "achieved": round(ach, 1), "peak": peak, "unit": unit,
+            "frac": round(ach / peak, 4), "peak_source": f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured"
+            else "fallback", "traffic": stored_traffic(stage, workload), "algorithmic_bytes": b,
+            "algorithmic_flops": f, "ms": round(ms, 4)}
+
+
+# ----------------------------------------------------------------------------- our implementation
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import expert_ffn_layer_gb300 as moe
+    import workloads as W
+    import __graft_entry__
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    moe.load()
+    pk, pk_kind = peaks()
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def f32(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def setup(name, replica_seed):
+        w = W.WORKLOADS[name]
+        t0 = time.time()
+        hidden_np, router_w, bias = W.router_inputs(w)
+        if replica_seed:  # each rank of a weak-scaling run has its own tokens, same weights
+            hidden_np = W.normal_bf16(w.seed + 1000 * replica_seed, W.TID_HIDDEN, (w.T, w.H), w.hidden_sigma)
+        gate, up, down = W.expert_weights(w)
+        sg, su, sd = W.shared_weights(w)
+        d = moe.dims(w.T, w.H, w.E, w.I, w.top_k, w.I_shared, w.score_mode, w.route_scale, w.renorm_eps,
+                     w.has_shared)
+        layer = moe.MoELayer(d, f32(router_w), f32(bias), bf(gate), bf(up), bf(down), bf(sg), bf(su), bf(sd))
+        del gate, up, down
+        hidden = bf(hidden_np)
+        log(f"[rank {rank}] {name}: inputs ready in {time.time() - t0:.1f}s")
+        return w, d, layer, hidden, hidden_np, (router_w, bias, sg, su, sd)
+
+    def timed(fn, K, W_):
+        for _ in range(W_):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record()
+            fn()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    def graph_of(fn, reps):
+        """A CUDA graph of `reps` back-to-back calls (no host gaps between kernels)."""
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()  # one eager call on the capture stream first
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                fn()
+        return g
+
+    def stage_times(w, d, layer, hidden, K):
+        """Each kernel of the layer on its own: a graph of K back-to-back launches of
+        that kernel, timed with events around the replay; ms per launch."""
+        S = w.T * w.top_k
+        idx = torch.empty((w.T, w.top_k), dtype=torch.int32, device=dev)
+        wts = torch.empty((w.T, w.top_k), dtype=torch.float32, device=dev)
+        counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+        offs = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(S, dtype=torch.int32, device=dev)
+        inv = torch.empty(S, dtype=torch.int32, device=dev)
+        y = torch.empty((S, w.H), dtype=torch.bfloat16, device=dev)
+        z = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+        ws = layer.ws
+        L = layer
+        calls = {
+            "route": lambda: moe.moe_route(d, hidden, L.router_w, L.expert_bias, idx, wts, ws),
+            "permute": lambda: moe.moe_permute(d, idx, counts, offs, perm, inv, ws),
+            "gate_up": lambda: moe.moe_expert_gate_up(d, hidden, perm, offs, L.w_gate, L.w_up, L.ws_gate, L.ws_up, ws),
+            "down": lambda: moe.moe_expert_down(d, offs, L.w_down, L.ws_down, y, z, ws),
+            "combine": lambda: moe.moe_combine(d, y, z, inv, wts, out),
+        }
+        for name in calls:  # produce every intermediate once, in order
+            calls[name]()
+        torch.cuda.synchronize()
+        times = {}
+        for name, fn in calls.items():
+            g = graph_of(fn, K)
+            g.replay()
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            times[name] = e0.elapsed_time(e1) / K
+            del g
+        n_active = int((counts > 0).sum().item())
+        return times, n_active, counts.cpu().numpy()
+
+    # ---------------- headline workload (decode, T = 8)
+    name = args.workload
+    w, d, layer, hidden, hidden_np, host = setup(name, rank)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    if args.profile:
+        for _ in range(args.warmup + 1):
+            layer(hidden, out)
+        torch.cuda.synchronize()
+        return {"profile": name, "device_error": moe.moe_ws_read_error(layer.ws)}
+
+    def eager_step():
+        layer(hidden, out)
+
+    # one layer forward captured as a CUDA graph (the library enqueues no host
+    # synchronisation and allocates nothing, so the whole chain captures)
+    layer_graph = graph_of(eager_step, 1)
+
+    def step():
+        layer_graph.replay()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        per_step = timed(step, args.steps, 0)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = max_over_ranks(float(np.sum(per_step)))
+    err = moe.moe_ws_read_error(layer.ws)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after the timed steps")
+    value = world * w.T * args.steps / (total_ms * 1e-3)
+    eager_ms = max_over_ranks(float(np.sum(timed(eager_step, args.steps, 1))))
+
+    # ---------------- end to end through MoELayer with host buffers
+    h_in = torch.from_numpy(np.ascontiguousarray(hidden_np).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_out = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        hidden.copy_(h_in, non_blocking=True)
+        layer(hidden, out)
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_ms = max_over_ranks(float(np.sum(timed(e2e_step, args.steps, max(1, args.warmup)))))
+    e2e_value = world * w.T * args.steps / (e2e_ms * 1e-3)
+
+    # ---------------- per-kernel durations -> roofline of the dominant kernel
+    st_ms, n_active, counts = stage_times(w, d, layer, hidden, args.steps)
+    work = stage_work(w, n_active)
+    dominant = max(st_ms, key=st_ms.get)
+    roof = roofline_for(dominant, work, st_ms[dominant], pk, pk_kind, f"{name}_T{w.T}", bound="hbm")
+    kernels = {n: {"ms": round(v, 4), **{kk: vv for kk, vv in roofline_for(n, work, v, pk, pk_kind,
+                                                                            f"{name}_T{w.T}").items()
+                                          if kk in ("bound", "achieved", "unit", "frac")}}
+               for n, v in st_ms.items()}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) hidden, N(0,0.02) bf16 expert weights, N(0,0.02) fp32 router, "
+                "N(0,0.1) expert bias (the pages' shapes; no trained weights)",
+        "config": {**w.describe(), "workload": f"hy3_{name}_T{w.T}", "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": "CUDA graph of one layer forward (5 kernels, PDL-chained)",
+                   "eager_ms_per_step": round(eager_ms / args.steps, 5),
+                   "active_experts": n_active, "max_tokens_per_expert": int(counts.max())},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": w.T * w.H * 2,
+                "d2h_bytes_per_step": w.T * w.H * 2, "ms_per_step": round(e2e_ms / args.steps, 5)},
+        "gpu_launches": 5 * args.steps,
+        "roofline": roof,
+        "kernels": kernels,
+        "clocks": clk.summary(),
+    }
+    del layer, hidden, layer_graph
+    torch.cuda.empty_cache()
+
+    # ---------------- prefill chunk (T = 4096), single GPU
+    if world == 1 and not args.no_prefill:
+        pw, pd, player, phidden, _, _ = setup("prefill", 0)
+        pout = torch.empty((pw.T, pw.H), dtype=torch.bfloat16, device=dev)
+        pgraph = graph_of(lambda: player(phidden, pout), 1)
+        pst = timed(pgraph.replay, args.steps, args.warmup)
+        pms = float(np.mean(pst))
+        pst_ms, pact, pcounts = stage_times(pw, pd, player, phidden, max(3, args.steps // 2))
+        pwork = stage_work(pw, pact)
+        flops = sum(v["flops"] for k, v in pwork.items() if k in ("gate_up", "down"))
+        wbytes = sum(pwork[k]["bytes"] for k in ("gate_up", "down"))
+        pdom = max(pst_ms, key=pst_ms.get)
+        result["prefill"] = {
+            "workload": f"hy3_prefill_T{pw.T}", "value": round(pw.T / (pms * 1e-3), 1), "unit": UNIT,
+            "ms_per_step": round(pms, 5), "active_experts": pact, "max_tokens_per_expert": int(pcounts.max()),
+            "layer_tensor_frac": round(flops / (pms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+            "layer_hbm_frac": round(wbytes / (pms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "roofline": roofline_for(pdom, pwork, pst_ms[pdom], pk, pk_kind, f"prefill_T{pw.T}"),
+            "kernels": {n: round(v, 4) for n, v in pst_ms.items()},
+            "gpu_launches": 5 * args.steps,
+        }
+        del player, phidden, pgraph
+        torch.cuda.empty_cache()
+
+    # ---------------- the oracle on the host cores (rank 0 only, N = 1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, hidden_np, budget_s=args.cpu_seconds)
+    return result
+
+
+# ----------------------------------------------------------------------------- the oracle as a baseline
+
+def _oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(w, hidden_np=None):
+    """The workload's inputs for the oracle; only the experts the batch reaches
+    are generated (the oracle touches no other expert)."""
+    import oracle
+    import workloads as W
+
+    key = (w.name, None if hidden_np is None else hash(hidden_np.tobytes()))
+    if key not in _ORACLE_INPUTS:
+        hid, router_w, bias = W.router_inputs(w)
+        if hidden_np is not None:
+            hid = hidden_np
+        logits = oracle.router_logits(hid, router_w)
+        r = oracle.route_sigmoid(logits, bias, w.top_k, w.route_scale) if w.score_mode == "sigmoid" \
+            else oracle.route_softmax(logits, w.top_k, w.renorm_eps)
+        gate, up, down = W.expert_weights(w, experts=np.unique(r["idx"]))
+        sg, su, sd = W.shared_weights(w)
+        _ORACLE_INPUTS.clear()
+        _ORACLE_INPUTS[key] = (hid, router_w, bias, gate, up, down, sg, su, sd)
+    return _ORACLE_INPUTS[key]
+
+
+def cpu_baseline(w, hidden_np=None, budget_s: float = 15.0, steps: int | None = None):
+    """Time the fp64 oracle (as it stands) on the same workload: whole layers of
+    the T-token batch, repeated until the time budget (or `steps` layers) is used."""
+    import oracle
+
+    hid, router_w, bias, gate, up, down, sg, su, sd = _oracle_inputs(w, hidden_np)
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        oracle.layer_forward(hid, router_w, bias, gate, up, down, sg, su, sd, top_k=w.top_k,
+                             score_mode=w.score_mode, route_scale=w.route_scale, renorm_eps=w.renorm_eps)
+        runs += 1
+        el = time.perf_counter() - t0
+        if (steps is not None and runs >= steps) or (steps is None and el >= budget_s):
+            break
+    return {"value": round(runs * w.T / el, 3), "unit": UNIT, "cores": _oracle_threads(), "kind": "oracle",
+            "sample": f"{runs} whole layer forwards of the {w.T}-token batch (fp64 numpy oracle), {el:.1f}s",
+            "seconds_per_layer": round(el / runs, 3)}
+
+
+def run_reference(args, world):
+    import workloads as W
+
+    w = W.WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        cpu_baseline(w, steps=1)
+    t0 = time.perf_counter()
+    cb = cpu_baseline(w, steps=args.steps)
+    el = time.perf_counter() - t0
+    value = cb["value"]
+    ms = 1e3 * el / args.steps
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded workload as the GPU arm)",
+        "config": {**w.describe(), "workload": f"hy3_{args.workload}_T{w.T}"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
+                         "sample": cb["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "prefill", "prefill_u", "zipf", "image", "decode_e48", "prefill_e32"])
+    ap.add_argument("--profile", action="store_true",
+                    help="only run warm-up layer forwards and one more (for hardware-counter captures)")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the T=4096 prefill measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, world)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

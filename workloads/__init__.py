@@ -169,6 +169,11 @@ WORKLOADS = {
     "prefill_u": _hy3("prefill_u", 4096, 2, bias_sigma=0.01),
     "zipf": _hy3("zipf", 16384, 3, bias="zipf"),
     "image": Workload("image", 8192, 4096, 64, 8, 3072, 3072, "softmax", 1.0, 1e-8, True, "none", 0.0, 4),
+    # profiling proxies: the same tile shapes with fewer experts resident (< 2 GB of
+    # weights), for hardware-counter captures that replay a kernel many times
+    "decode_e48": Workload("decode_e48", 8, 4096, 48, 8, 1536, 1536, "sigmoid", 2.826, 0.0, True, "normal", 0.1, 1),
+    "prefill_e32": Workload("prefill_e32", 704, 4096, 32, 8, 1536, 1536, "sigmoid", 2.826, 0.0, True, "normal", 0.1,
+                            2),
 }
 
 
