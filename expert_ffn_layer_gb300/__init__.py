@@ -31,7 +31,7 @@ SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
 
 EXPORTS = ("moe_status_string", "moe_check_dims", "moe_workspace_bytes", "moe_ws_init", "moe_ws_read_error",
            "moe_route", "moe_permute", "moe_expert_ffn", "moe_expert_gate_up", "moe_expert_down", "moe_combine",
-           "moe_layer_forward")
+           "moe_layer_forward", "moe_expert_ffn_noalloc")
 
 
 class MoeError(RuntimeError):

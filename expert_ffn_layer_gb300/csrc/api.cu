@@ -447,3 +447,63 @@ MOE_API moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, 
     return st;
   return do_combine(*d, y, z, inv, w, out, s, true);
 }
+
+// ---------------------------------------------------------------------------
+// moe_expert_ffn_noalloc: moe_expert_ffn for callers that cannot allocate
+// device memory.  Its scratch (the error word and the bf16 activations between
+// the gate/up and the down GEMM) lives in the file-scope array below instead
+// of a caller-provided workspace.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB, held on every device that loads this library
+__device__ __align__(256) static unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 128;
+std::mutex g_scratch_mutex;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the array on the current device (the host-side name is not
+// one).  Looked up once per device, on that device's first call.
+void *static_scratch(cudaError_t *err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_scratch_ptr[dev] = p;
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+MOE_API moe_status moe_expert_ffn_noalloc(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
+                                          const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                                          const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
+                                          const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared,
+                                          void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(hidden) || !ptr_ok(perm) || !ptr_ok(offsets) || !ptr_ok(w_gate) || !ptr_ok(w_up) || !ptr_ok(w_down) ||
+      !ptr_ok(y_sorted))
+    return MOE_ERR_INVALID_ARG;
+  if (d->has_shared && (!ptr_ok(ws_gate) || !ptr_ok(ws_up) || !ptr_ok(ws_down) || !ptr_ok(y_shared)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_layout(*d).total > kStaticScratchBytes) return MOE_ERR_WORKSPACE;  // beyond the built-in scratch
+  cudaError_t e = cudaSuccess;
+  void *ws = static_scratch(&e);
+  if (ws == nullptr) return MOE_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  // the array keeps the previous call's contents: the header (error word) must start at zero
+  if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return do_expert_ffn(*d, hidden, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_sorted, y_shared,
+                       ws, s, true);
+}

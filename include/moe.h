@@ -168,6 +168,29 @@ moe_status moe_expert_down(const moe_dims *d, const int32_t *offsets, const moe_
                            const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws,
                            size_t ws_bytes, void *stream);
 
+/* moe_expert_ffn for callers that cannot allocate device memory: a plugin
+ * running inside a host framework that owns every device allocation and hands
+ * its plugins none, or a latency-critical serving loop that must not call
+ * cudaMalloc once it is running (cudaMalloc can synchronise the device).  It
+ * takes no workspace: its scratch is a 32 MiB array that this library keeps in
+ * device memory on every GPU that loads it, until the process exits.  There is
+ * no counterpart on the pages: this is an interface convenience, not a step of
+ * the layer.
+ *   Arguments and results as for moe_expert_ffn (the caller still passes every
+ *   input and output).  Dims whose moe_workspace_bytes() exceeds 32 MiB are
+ *   rejected with MOE_ERR_WORKSPACE before anything is launched (for the Hy3
+ *   shape that admits batches up to about T = 300 tokens).
+ *   The first call on a device looks up that device's address of the array
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call uses the same array: calls that overlap on the device (two
+ *   streams, or two host threads) race and give wrong results; serialise them.
+ *   Device-side anomalies are not reported on this path (the error word is
+ *   cleared at the start of every call). */
+moe_status moe_expert_ffn_noalloc(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
+                                  const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                                  const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
+                                  const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *stream);
+
 /* Step a9: out[t] = sum_j topk_w[t, j] * y_sorted[inv_perm[t * top_k + j]] + y_shared[t]
  * (fp32 sum in j order, one bf16 rounding).  [case] section 3 (top-k weighted
  * aggregation at the end); [image] Routed Experts (weighted sum over k) and
