@@ -138,7 +138,8 @@ def stage_work(w, n_active: int):
     Ts = T if w.has_shared else 0
     ns = 1 if w.has_shared else 0
     return {
-        "route": {"bytes": E * H * 4 + T * H * 2 + S * 8 + E * 4, "flops": 2 * 2 * T * H * E},
+        # route = split (E*H fp32 -> 2 x bf16) + router GEMM (x, W_high, W_low) + top-k
+        "route": {"bytes": E * H * 4 + 2 * E * H * 2 + T * H * 2 + S * 8 + E * 4, "flops": 2 * 2 * T * H * E},
         "permute": {"bytes": S * 4 * 3 + (2 * E + 1) * 4, "flops": 0},
         "gate_up": {"bytes": (n_active * 2 * I + ns * 2 * Is) * H * 2 + (S + Ts) * H * 2 + (S * I + Ts * Is) * 2,
                     "flops": 4 * (S * H * I + Ts * H * Is)},
@@ -349,12 +350,12 @@ def run_ours(args, rank, world, local_rank):
                 "N(0,0.1) expert bias (the pages' shapes; no trained weights)",
         "config": {**w.describe(), "workload": f"hy3_{name}_T{w.T}", "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "CUDA graph of one layer forward (5 kernels, PDL-chained)",
+                   "launch": "CUDA graph of one layer forward (7 kernels, PDL-chained)",
                    "eager_ms_per_step": round(eager_ms / args.steps, 5),
                    "active_experts": n_active, "max_tokens_per_expert": int(counts.max())},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": w.T * w.H * 2,
                 "d2h_bytes_per_step": w.T * w.H * 2, "ms_per_step": round(e2e_ms / args.steps, 5)},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 7 * args.steps,  # split, router gemm, top-k, permute, gate/up, down, combine
         "roofline": roof,
         "kernels": kernels,
         "clocks": clk.summary(),
@@ -381,7 +382,7 @@ def run_ours(args, rank, world, local_rank):
             "layer_hbm_frac": round(wbytes / (pms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
             "roofline": roofline_for(pdom, pwork, pst_ms[pdom], pk, pk_kind, f"prefill_T{pw.T}"),
             "kernels": {n: round(v, 4) for n, v in pst_ms.items()},
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": 7 * args.steps,  # split, router gemm, top-k, permute, gate/up, down, combine
         }
         del player, phidden, pgraph
         torch.cuda.empty_cache()

@@ -90,8 +90,20 @@ inline bool aligned256(const void *p) { return ((uintptr_t)p & 255u) == 0; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t err, topk_idx, topk_w, counts, offsets, perm, inv, y_sorted, y_shared, a_act, a_shared, total;
+  size_t err, topk_idx, topk_w, counts, offsets, perm, inv, y_sorted, y_shared, a_act, a_shared, w_hi, w_lo, partial,
+      total;
 };
+
+// Split of H across router CTAs: a power of two <= 32 dividing H/64, with
+// ksplit x (T/128 tiles) about the SM count.  With nsm = 256 it bounds every
+// device's choice, which sizes the workspace without a device query.
+int router_ksplit(const moe_dims &d, int nsm) {
+  const int mtiles = (d.T + 127) / 128;
+  const int nslices = d.H / 64;
+  int ks = 32;
+  while (ks > 1 && ((long long)mtiles * ks > nsm || nslices % ks != 0)) ks >>= 1;
+  return ks;
+}
 
 WsLayout ws_layout(const moe_dims &d) {
   WsLayout L;
@@ -114,6 +126,9 @@ WsLayout ws_layout(const moe_dims &d) {
   L.y_shared = take(d.has_shared ? T * (size_t)d.H * 2 : 0);
   L.a_act = take(S * (size_t)d.I * 2);
   L.a_shared = take(T * Is * 2);
+  L.w_hi = take(E * (size_t)d.H * 2);
+  L.w_lo = take(E * (size_t)d.H * 2);
+  L.partial = take((size_t)router_ksplit(d, 256) * T * E * 4);
   L.total = off;
   return L;
 }
@@ -144,21 +159,19 @@ moe_status check_ws(const moe_dims *d, void *ws, size_t ws_bytes) {
 
 // ------------------------------------------------------------ stages
 moe_status do_route(const moe_dims &d, const moe_bf16 *hidden, const float *router_w, const float *bias,
-                    float *logits_out, int32_t *topk_idx, float *topk_w, unsigned *err, cudaStream_t stream,
-                    bool pdl) {
+                    float *logits_out, int32_t *topk_idx, float *topk_w, void *ws, cudaStream_t stream, bool pdl) {
+  const WsLayout L = ws_layout(d);
   RouterParams p;
   std::memset(&p, 0, sizeof(p));
-  p.err = err;
   const int Epad = (d.E + 15) & ~15;
-  if (!map_bf16_2d(&p.map_x, hidden, (uint64_t)d.H, (uint64_t)d.T, 128)) return MOE_ERR_CUDA;
-  {
-    const uint64_t dims[2] = {(uint64_t)d.H, (uint64_t)d.E};
-    const uint64_t str[1] = {(uint64_t)d.H * 4};
-    const uint32_t box[2] = {64, (uint32_t)Epad};
-    if (!encode(&p.map_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, router_w, dims, str, box,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
-      return MOE_ERR_CUDA;
-  }
+  p.w_hi = at<__nv_bfloat16>(ws, L.w_hi);
+  p.w_lo = at<__nv_bfloat16>(ws, L.w_lo);
+  p.partial = at<float>(ws, L.partial);
+  p.err = at<unsigned>(ws, L.err);
+  if (!map_bf16_2d(&p.map_x, hidden, (uint64_t)d.H, (uint64_t)d.T, 128) ||
+      !map_bf16_2d(&p.map_hi, p.w_hi, (uint64_t)d.H, (uint64_t)d.E, (uint32_t)Epad) ||
+      !map_bf16_2d(&p.map_lo, p.w_lo, (uint64_t)d.H, (uint64_t)d.E, (uint32_t)Epad))
+    return MOE_ERR_CUDA;
   p.bias = d.score_mode == MOE_SCORE_SIGMOID_BIAS ? bias : nullptr;
   p.logits_out = logits_out;
   p.topk_idx = topk_idx;
@@ -173,11 +186,9 @@ moe_status do_route(const moe_dims &d, const moe_bf16 *hidden, const float *rout
   p.renorm_eps = d.renorm_eps;
   p.stages = router_stages(Epad);
   const int mtiles = (d.T + 127) / 128;
-  const int nslices = d.H / 64;
-  int ks = 8;
-  while (ks > 1 && ((long long)mtiles * ks > num_sms() || nslices % ks != 0)) ks >>= 1;
-  p.kslices_per_cta = nslices / ks;
-  return cuda_status(launch_router(p, ks, mtiles, stream, pdl));
+  const int ks = router_ksplit(d, num_sms());
+  p.kslices_per_cta = (d.H / 64) / ks;
+  return cuda_status(launch_router(p, router_w, ks, mtiles, stream, pdl));
 }
 
 moe_status do_permute(const moe_dims &d, const int32_t *topk_idx, int32_t *counts, int32_t *offsets, int32_t *perm,
@@ -218,11 +229,11 @@ moe_status do_gate_up(const moe_dims &d, const moe_bf16 *hidden, const int32_t *
                       void *ws, cudaStream_t stream, bool pdl) {
   const WsLayout L = ws_layout(d);
   GemmParams g = gemm_common(d, perm, offsets, ws);
-  bool ok = map_bf16_3d(&g.map_a0, w_gate, d.H, d.I, d.E, 16) && map_bf16_3d(&g.map_a1, w_up, d.H, d.I, d.E, 16) &&
-            map_bf16_2d(&g.map_b, hidden, d.H, d.T, 1);
+  bool ok = map_bf16_3d(&g.map_a0, w_gate, d.H, d.I, d.E, 128) && map_bf16_3d(&g.map_a1, w_up, d.H, d.I, d.E, 128);
   if (d.has_shared)
-    ok = ok && map_bf16_2d(&g.map_s0, ws_gate, d.H, g.Is, 16) && map_bf16_2d(&g.map_s1, ws_up, d.H, g.Is, 16);
+    ok = ok && map_bf16_2d(&g.map_s0, ws_gate, d.H, g.Is, 128) && map_bf16_2d(&g.map_s1, ws_up, d.H, g.Is, 128);
   if (!ok) return MOE_ERR_CUDA;
+  g.hidden = reinterpret_cast<const __nv_bfloat16 *>(hidden);
   g.out = at<__nv_bfloat16>(ws, L.a_act);
   g.out_s = at<__nv_bfloat16>(ws, L.a_shared);
   return cuda_status(launch_expert_gemm(g, kGateUp, gemm_tile_n(d.T), num_sms(), stream, pdl));
@@ -233,11 +244,13 @@ moe_status do_down(const moe_dims &d, const int32_t *offsets, const moe_bf16 *w_
                    moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl) {
   const WsLayout L = ws_layout(d);
   GemmParams h = gemm_common(d, nullptr, offsets, ws);
-  bool ok = map_bf16_3d(&h.map_a0, w_down, d.I, d.H, d.E, 128) &&
-            map_bf16_2d(&h.map_b, at<moe_bf16>(ws, L.a_act), d.I, h.S, 16);
-  if (d.has_shared)
-    ok = ok && map_bf16_2d(&h.map_s0, ws_down, h.Is, d.H, 128) &&
-         map_bf16_2d(&h.map_bs, at<moe_bf16>(ws, L.a_shared), h.Is, d.T, 16);
+  bool ok = map_bf16_3d(&h.map_a0, w_down, d.I, d.H, d.E, 128);
+  for (int b = 0; b < 4; ++b) ok = ok && map_bf16_2d(&h.map_b[b], at<moe_bf16>(ws, L.a_act), d.I, h.S, 16u << b);
+  if (d.has_shared) {
+    ok = ok && map_bf16_2d(&h.map_s0, ws_down, h.Is, d.H, 128);
+    for (int b = 0; b < 4; ++b)
+      ok = ok && map_bf16_2d(&h.map_bs[b], at<moe_bf16>(ws, L.a_shared), h.Is, d.T, 16u << b);
+  }
   if (!ok) return MOE_ERR_CUDA;
   h.out = reinterpret_cast<__nv_bfloat16 *>(y_sorted);
   h.out_s = reinterpret_cast<__nv_bfloat16 *>(y_shared);
@@ -335,13 +348,8 @@ MOE_API moe_status moe_route(const moe_dims *d, const moe_bf16 *hidden, const fl
   if (!ptr_ok(hidden) || !ptr_ok(router_w) || !ptr_ok(topk_idx) || !ptr_ok(topk_w)) return MOE_ERR_INVALID_ARG;
   if ((expert_bias != nullptr && !aligned16(expert_bias)) || (logits_out != nullptr && !aligned16(logits_out)))
     return MOE_ERR_INVALID_ARG;
-  // the workspace is optional here: when given, device-side anomalies are recorded in its error word
-  unsigned *err = nullptr;
-  if (ws != nullptr) {
-    if (!aligned256(ws) || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
-    err = at<unsigned>(ws, 0);
-  }
-  return do_route(*d, hidden, router_w, expert_bias, logits_out, topk_idx, topk_w, err, (cudaStream_t)stream, true);
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  return do_route(*d, hidden, router_w, expert_bias, logits_out, topk_idx, topk_w, ws, (cudaStream_t)stream, true);
 }
 
 MOE_API moe_status moe_permute(const moe_dims *d, const int32_t *topk_idx, int32_t *counts, int32_t *offsets,
@@ -436,9 +444,7 @@ MOE_API moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, 
   int32_t *perm = at<int32_t>(ws, L.perm), *inv = at<int32_t>(ws, L.inv);
   int32_t *offs = at<int32_t>(ws, L.offsets);
   moe_bf16 *y = at<moe_bf16>(ws, L.y_sorted), *z = at<moe_bf16>(ws, L.y_shared);
-  if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, w, at<unsigned>(ws, L.err), s, true)) !=
-      MOE_OK)
-    return st;
+  if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, w, ws, s, true)) != MOE_OK) return st;
   if ((st = do_permute(*d, idx, at<int32_t>(ws, L.counts), offs, perm, inv, at<unsigned>(ws, L.err), s, true)) !=
       MOE_OK)
     return st;

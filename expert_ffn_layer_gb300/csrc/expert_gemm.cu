@@ -7,25 +7,32 @@
 // SwiGLU experts down(SiLU(gate(x)) * up(x)), stacked expert weights, the
 // shared MLP applied to every token.
 //
-// Orientation ("swap AB"): the weight rows are the M = 128 operand and the
-// tokens of one expert chunk are the N operand (N = tokens rounded up to 16,
-// at most BN), so an expert with a handful of tokens (decode) costs one
-// narrow MMA per K step while its weights stream at full rate, and large
-// segments pad to 16 tokens instead of 128.
+// Orientation: weight rows are the M = 128 operand of every MMA and the tokens
+// of one expert chunk are the N operand (N = tokens rounded up to 16, at most
+// BN <= 256).  A tile is 256 weight rows x N tokens: two MMAs per K step share
+// one token tile and accumulate into two TMEM accumulators,
+//   gate/up: D0 = gate rows i0..i0+127, D1 = up rows i0..i0+127, so gate row i
+//            and up row i land in the same TMEM lane and one thread forms
+//            SiLU(gate) * up -> bf16 activation A_act[p][i];
+//   down:    D0 = w_down rows h0..h0+127, D1 = rows h0+128..h0+255 -> y[p][h].
+// Sharing the token tile between 256 weight rows halves the token re-reads
+// from L2 compared with one 128-row MMA per tile.
 //
-//   gate/up tile: A = [16 gate rows | 16 up rows] x 4 (rows i0..i0+63 of both
-//     matrices, interleaved so that gate row i and up row i sit 16 TMEM lanes
-//     apart in the same warp), B = token rows gathered with TMA gather4 via
-//     perm[p] / k; epilogue: SiLU(gate) * up -> bf16 activation A_act[p][i].
-//   down tile:    A = 128 rows of w_down (h0..h0+127), B = A_act rows of the
-//     chunk (contiguous); epilogue -> bf16 y_sorted[p][h].
+// Operand loads per 64-wide K step: the two 128-row weight boxes by TMA
+// (128-byte swizzle); the token rows of gate/up through the route index
+// (token = perm[p] / k) by cp.async from 128 producer threads straight from
+// `hidden`, written in the same swizzled layout (TMA's row-gather moves 4 rows
+// per instruction and tops out far below the rate these tiles need); the
+// activation rows of down, which are contiguous, by at most four TMA boxes.
 //
 // Persistent CTAs (one per SM) walk the tile list in a static stride; the
-// tile list (per segment: chunks of <= BN tokens x weight row blocks) is
-// derived in every CTA from the expert offsets.  Warp roles: 0 TMA producer,
-// 1 tcgen05.mma issuer (one thread), 2-5 epilogue (TMEM -> registers ->
-// global).  A STAGES-deep shared-memory ring and two TMEM accumulators let
-// loads, MMAs and the epilogue of consecutive tiles overlap.
+// tile list (per segment: weight row blocks x chunks of <= BN tokens, chunks
+// innermost so chunks of one row block reuse its weights in L2) is derived in
+// every CTA from the expert offsets.  Warp roles: 0-3 producers, 4 MMA issuer
+// (one thread) and TMEM owner, 5-8 epilogue.  A STAGES-deep shared-memory
+// ring overlaps loads and MMAs; for BN <= 128 two TMEM accumulator pairs also
+// overlap one tile's epilogue with the next tile's MMAs (BN = 256 fills TMEM
+// with one pair).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -33,19 +40,16 @@ namespace moe {
 
 namespace {
 
-constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
-constexpr int kMaxSeg = 258;        // E <= 256 routed + 1 shared (+1 sentinel)
+constexpr int kABytes = 2 * 128 * 128;  // two 128-row x 64-bf16 weight boxes
+constexpr int kMaxSeg = 258;            // E <= 256 routed + 1 shared (+1 sentinel)
+constexpr int kProducers = 128;         // warps 0-3
+constexpr int kMmaWarp = 4;
 constexpr unsigned long long kDrainNs = 20000000ull;
 
 template <int BN>
 struct StagesFor {
-  static constexpr int value = BN <= 16 ? 12 : BN <= 32 ? 10 : BN <= 64 ? 8 : BN <= 128 ? 6 : 4;
+  static constexpr int value = BN <= 32 ? 6 : BN <= 64 ? 5 : BN <= 128 ? 4 : 3;
 };
-
-template <int BN>
-constexpr int tmem_cols_for() {
-  return (2 * BN) < 32 ? 32 : 2 * BN;
-}
 
 template <int MODE, int BN>
 struct Layout {
@@ -58,6 +62,12 @@ struct Layout {
   static constexpr int kOffOff = kStartOff + 4 * kMaxSeg;
   static constexpr int kBytes = kOffOff + 4 * kMaxSeg;
   static constexpr size_t kSmem = 1024 + kBytes;
+  // accumulator pairs of 2 x BN columns: two (MMA of the next tile overlaps the
+  // epilogue of this one) while they fit in the 512 TMEM columns, else one
+  static constexpr int kAccBufs = 4 * BN <= 512 ? 2 : 1;
+  static constexpr uint32_t kTmemCols = kAccBufs * 2 * BN;
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM budget");
 };
 
 struct Tile {
@@ -72,11 +82,18 @@ __device__ __forceinline__ int chunk_base(int cnt) {
   const int per = (cnt + n0 - 1) / n0;
   return (per + 15) & ~15;
 }
+template <int BN>
+__device__ __forceinline__ int chunk_count(int cnt) {
+  if (cnt <= 0) return 0;
+  const int b = chunk_base<BN>(cnt);
+  return (cnt + b - 1) / b;
+}
 
+// Weight row blocks of a segment: 128 gate/up pairs, or 256 rows of w_down.
 template <int MODE>
 __device__ __forceinline__ int seg_nrb(const GemmParams &p, bool shared) {
-  if (MODE == kGateUp) return (shared ? p.Is : p.I) >> 6;
-  return (p.H + 127) >> 7;
+  if (MODE == kGateUp) return ((shared ? p.Is : p.I) + 127) >> 7;
+  return (p.H + 255) >> 8;
 }
 
 template <int MODE, int BN>
@@ -92,10 +109,10 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const in
   tl.seg = lo;
   tl.shared = (lo == p.E) ? 1 : 0;
   const int cnt = tl.shared ? p.T : seg_off[lo + 1] - seg_off[lo];
-  const int nrb = seg_nrb<MODE>(p, tl.shared);
+  const int nch = chunk_count<BN>(cnt);
   const int local = t - tile_start[lo];
-  const int ch = local / nrb;
-  tl.rb = local - ch * nrb;
+  tl.rb = local / nch;
+  const int ch = local - tl.rb * nch;
   const int base = chunk_base<BN>(cnt);
   const int pin = ch * base;
   tl.ntok = min(base, cnt - pin);
@@ -112,13 +129,24 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed (the
+// arrival is one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
 }  // namespace
 
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __grid_constant__ GemmParams p) {
   using L = Layout<MODE, BN>;
   constexpr int STAGES = L::kStages;
-  constexpr uint32_t kTmemCols = tmem_cols_for<BN>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = (uint64_t *)(smem + L::kBarOff);
@@ -138,7 +166,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      // gate/up: 128 cp.async arrivals + the TMA expect_tx arrival; down: TMA only
+      mbar_init(full_bar(s), MODE == kGateUp ? kProducers + 1 : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -151,12 +180,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.map_a0);
-    tma_prefetch_desc(&p.map_b);
     if (MODE == kGateUp) tma_prefetch_desc(&p.map_a1);
     if (p.has_shared) tma_prefetch_desc(&p.map_s0);
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -167,9 +195,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
   pdl_wait();  // perm / offsets / activations come from the previous kernel
   pdl_launch_dependents();
 
-  // ---------------- tile list from the expert offsets (warp 2)
+  // ---------------- tile list from the expert offsets (one warp)
   const int nseg = p.E + (p.has_shared ? 1 : 0);
-  if (warp == 2) {
+  if (warp == kMmaWarp) {
     for (int i = lane; i <= p.E; i += 32) seg_off[i] = __ldg(p.offsets + i);
     __syncwarp();
     bool good = true;
@@ -186,8 +214,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
     for (int s = s0; s < min(nseg, s0 + per); ++s) {
       const bool sh = (s == p.E);
       const int cnt = sh ? p.T : seg_off[s + 1] - seg_off[s];
-      const int chunks = cnt > 0 ? (cnt + chunk_base<BN>(cnt) - 1) / chunk_base<BN>(cnt) : 0;
-      local += good ? chunks * seg_nrb<MODE>(p, sh) : 0;
+      local += good ? chunk_count<BN>(cnt) * seg_nrb<MODE>(p, sh) : 0;
     }
     int incl = local;
 #pragma unroll
@@ -200,8 +227,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
       tile_start[s] = run;
       const bool sh = (s == p.E);
       const int cnt = sh ? p.T : seg_off[s + 1] - seg_off[s];
-      const int chunks = cnt > 0 ? (cnt + chunk_base<BN>(cnt) - 1) / chunk_base<BN>(cnt) : 0;
-      run += good ? chunks * seg_nrb<MODE>(p, sh) : 0;
+      run += good ? chunk_count<BN>(cnt) * seg_nrb<MODE>(p, sh) : 0;
     }
     if (lane == 31) tile_start[nseg] = incl;
   }
@@ -210,27 +236,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
   unsigned *err = p.err;
   bool ok = true;
 
-  if (warp == 0) {
-    // ================= TMA producer
+  if (warp < 4) {
+    // ================= producers
+    const bool tma_thread = threadIdx.x == 0;
     const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_x = policy_evict_last();
     int st = 0;
     uint32_t ph = 0;
-    uint32_t issued = 0, issued_par = 0;  // per stage: has a load been issued, and its phase parity
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = decode_tile<MODE, BN>(p, t, tile_start, seg_off, nseg);
-      int rows[8];
-      bool bad = false;
-      if (MODE == kGateUp) {
+    uint32_t issued = 0, issued_par = 0;  // per stage: TMA issued, and its phase parity (thread 0)
+    if (MODE == kGateUp || warp == 0) {
+      const int tid = threadIdx.x;          // 0..127
+      const int c8 = tid & 7, rbase = tid >> 3;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<MODE, BN>(p, t, tile_start, seg_off, nseg);
+        // token rows of this thread (gate/up): rows rbase + 16 j of the chunk
+        const __nv_bfloat16 *src[BN / 16];
+        if (MODE == kGateUp) {
+          bool bad = false;
 #pragma unroll
-        for (int gi = 0; gi < 2; ++gi) {
-          const int g = lane + 32 * gi;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r = 4 * g + q;
+          for (int j = 0; j < BN / 16; ++j) {
+            const int r = rbase + 16 * j;
             const int rr = r < tl.ntok ? r : 0;
             int tok = 0;
-            if (g * 4 < tl.N) {
+            if (r < tl.N) {
               if (tl.shared) {
                 tok = tl.row0 + rr;
               } else {
@@ -242,69 +269,78 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
                 }
               }
             }
-            rows[gi * 4 + q] = tok;
+            src[j] = p.hidden + (size_t)tok * p.H + c8 * 8;
           }
+          if (bad && err != nullptr) atomicOr(err, MOE_DEVERR_INDEX);
         }
-        if (bad && err != nullptr) atomicOr(err, MOE_DEVERR_INDEX);
-      }
-      const uint32_t tx = (uint32_t)(kABytes + tl.N * 128);
-      for (int kb = 0; kb < tl.nk; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(st), ph ^ 1u, err, abort_flag));
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full_bar(st), tx);
-          issued |= 1u << st;
-          issued_par = (issued_par & ~(1u << st)) | (ph << st);
-        }
-        __syncwarp();
-        const int k0 = kb * 64;
-        if (lane == 0) {
-          if (MODE == kGateUp) {
-            const int i0 = tl.rb * 64;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t dg = a_smem(st) + (uint32_t)(32 * q) * 128;
-              const uint32_t du = dg + 16 * 128;
+        const int i0 = tl.rb * (MODE == kGateUp ? 128 : 256);
+        for (int kb = 0; kb < tl.nk; ++kb) {
+          ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(st), ph ^ 1u, err, abort_flag));
+          if (!ok) break;
+          const int k0 = kb * 64;
+          if (tma_thread) {
+            const uint32_t tx = MODE == kGateUp ? (uint32_t)kABytes : (uint32_t)(kABytes + tl.N * 128);
+            mbar_arrive_expect_tx(full_bar(st), tx);
+            issued |= 1u << st;
+            issued_par = (issued_par & ~(1u << st)) | (ph << st);
+            const uint32_t a0 = a_smem(st), a1 = a0 + 16384;
+            if (MODE == kGateUp) {
               if (tl.shared) {
-                tma_load_2d_hint(dg, &p.map_s0, full_bar(st), k0, i0 + 16 * q, pol_w);
-                tma_load_2d_hint(du, &p.map_s1, full_bar(st), k0, i0 + 16 * q, pol_w);
+                tma_load_2d_hint(a0, &p.map_s0, full_bar(st), k0, i0, pol_w);
+                tma_load_2d_hint(a1, &p.map_s1, full_bar(st), k0, i0, pol_w);
               } else {
-                tma_load_3d_hint(dg, &p.map_a0, full_bar(st), k0, i0 + 16 * q, tl.seg, pol_w);
-                tma_load_3d_hint(du, &p.map_a1, full_bar(st), k0, i0 + 16 * q, tl.seg, pol_w);
+                tma_load_3d_hint(a0, &p.map_a0, full_bar(st), k0, i0, tl.seg, pol_w);
+                tma_load_3d_hint(a1, &p.map_a1, full_bar(st), k0, i0, tl.seg, pol_w);
+              }
+            } else {
+              if (tl.shared) {
+                tma_load_2d_hint(a0, &p.map_s0, full_bar(st), k0, i0, pol_w);
+                tma_load_2d_hint(a1, &p.map_s0, full_bar(st), k0, i0 + 128, pol_w);
+              } else {
+                tma_load_3d_hint(a0, &p.map_a0, full_bar(st), k0, i0, tl.seg, pol_w);
+                tma_load_3d_hint(a1, &p.map_a0, full_bar(st), k0, i0 + 128, tl.seg, pol_w);
+              }
+              // activation rows row0 .. row0 + N (contiguous, N a multiple of 16 and
+              // <= 256): boxes of 128 rows while they fit, then one each of 64/32/16
+              const CUtensorMap *mb = tl.shared ? p.map_bs : p.map_b;
+              int off = 0;
+              while (tl.N - off >= 128) {
+                tma_load_2d(b_smem(st) + (uint32_t)off * 128, &mb[3], full_bar(st), k0, tl.row0 + off);
+                off += 128;
+              }
+#pragma unroll
+              for (int bi = 2; bi >= 0; --bi) {
+                const int h = 16 << bi;
+                if (tl.N - off >= h) {
+                  tma_load_2d(b_smem(st) + (uint32_t)off * 128, &mb[bi], full_bar(st), k0, tl.row0 + off);
+                  off += h;
+                }
               }
             }
-          } else {
-            const int h0 = tl.rb * 128;
-            if (tl.shared) tma_load_2d_hint(a_smem(st), &p.map_s0, full_bar(st), k0, h0, pol_w);
-            else tma_load_3d_hint(a_smem(st), &p.map_a0, full_bar(st), k0, h0, tl.seg, pol_w);
           }
-        }
-        if (MODE == kGateUp) {
+          if (MODE == kGateUp) {
+            const uint32_t bs = b_smem(st);
 #pragma unroll
-          for (int gi = 0; gi < 2; ++gi) {
-            const int g = lane + 32 * gi;
-            if (g * 4 < tl.N)
-              tma_gather4(b_smem(st) + (uint32_t)g * 512, &p.map_b, full_bar(st), k0, rows[gi * 4 + 0],
-                          rows[gi * 4 + 1], rows[gi * 4 + 2], rows[gi * 4 + 3], pol_x);
+            for (int j = 0; j < BN / 16; ++j) {
+              const int r = rbase + 16 * j;
+              if (r < tl.N) cp_async_16(bs + r * 128 + ((c8 ^ (r & 7)) << 4), src[j] + k0);
+            }
+            cp_async_arrive_noinc(full_bar(st));
           }
-        } else {
-          if (lane * 16 < tl.N) {
-            const CUtensorMap *mb = tl.shared ? &p.map_bs : &p.map_b;
-            tma_load_2d_hint(b_smem(st) + (uint32_t)lane * 2048, mb, full_bar(st), k0, tl.row0 + 16 * lane, pol_x);
+          if (++st == STAGES) {
+            st = 0;
+            ph ^= 1u;
           }
-        }
-        if (++st == STAGES) {
-          st = 0;
-          ph ^= 1u;
         }
       }
+      if (!ok) {
+        if (MODE == kGateUp) cp_async_wait_all();
+        if (tma_thread)
+          for (int s = 0; s < STAGES; ++s)
+            if ((issued >> s) & 1u) mbar_wait_drain(full_bar(s), (issued_par >> s) & 1u);
+      }
     }
-    if (!ok && lane == 0) {
-      // let every load this CTA issued land before the block exits
-      for (int s = 0; s < STAGES; ++s)
-        if ((issued >> s) & 1u) mbar_wait_drain(full_bar(s), (issued_par >> s) & 1u);
-    }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ================= MMA issuer
     if (lane == 0) {
       int st = 0, it = 0;
@@ -312,22 +348,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
       bool any = false;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
         const Tile tl = decode_tile<MODE, BN>(p, t, tile_start, seg_off, nseg);
-        const int acc = it & 1;
-        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+        const int acc = it % L::kAccBufs;
+        const uint32_t aph = (uint32_t)(it / L::kAccBufs) & 1u;
         ok = mbar_wait(tempty_bar(acc), aph ^ 1u, err, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(acc * BN);
+        const uint32_t d0 = tmem + (uint32_t)(acc * 2 * BN);
+        const uint32_t d1 = d0 + (uint32_t)BN;
         const uint32_t idesc = idesc_bf16(128, tl.N);
         for (int kb = 0; kb < tl.nk; ++kb) {
           ok = mbar_wait(full_bar(st), ph, err, abort_flag);
           if (!ok) break;
+          if (MODE == kGateUp) fence_proxy_async_smem();  // token rows were written by cp.async
           tc_fence_after();
-          const uint64_t ad = sdesc_sw128(a_smem(st));
+          const uint64_t a0 = sdesc_sw128(a_smem(st));
+          const uint64_t a1 = sdesc_sw128(a_smem(st) + 16384);
           const uint64_t bd = sdesc_sw128(b_smem(st));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            umma_bf16(d0, a0 + 2 * kk, bd + 2 * kk, idesc, accum);
+            umma_bf16(d1, a1 + 2 * kk, bd + 2 * kk, idesc, accum);
+          }
           any = true;
           umma_commit(empty_bar(st));
           if (++st == STAGES) {
@@ -344,48 +386,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
       }
     }
   } else {
-    // ================= epilogue (warps 2..5 -> TMEM lane quarters 2,3,0,1)
+    // ================= epilogue (warps 5..8 -> TMEM lane quarters 1,2,3,0)
     const int q = warp & 3;
+    const int r = 32 * q + lane;  // weight row within the 128-row half
     int it = 0;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
       const Tile tl = decode_tile<MODE, BN>(p, t, tile_start, seg_off, nseg);
-      const int acc = it & 1;
-      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      const int acc = it % L::kAccBufs;
+      const uint32_t aph = (uint32_t)(it / L::kAccBufs) & 1u;
       ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, err, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * 2 * BN);
       if (MODE == kGateUp) {
         const int ld = tl.shared ? p.Is : p.I;
         __nv_bfloat16 *out = tl.shared ? p.out_s : p.out;
-        const int i = tl.rb * 64 + 16 * q + (lane & 15);
-        const bool upper = lane >= 16;
+        const int i = tl.rb * 128 + r;
         for (int c = 0; c < tl.N; c += 16) {
-          float v[16];
-          tmem_ld16(taddr + (uint32_t)c, v);
+          float g[16], u[16];
+          tmem_ld16(t0 + (uint32_t)c, g);
+          tmem_ld16(t0 + (uint32_t)(BN + c), u);
           tmem_wait_ld();
+          if (i < ld) {
 #pragma unroll
-          for (int j = 0; j < 16; j += 2) {
-            const float send = upper ? v[j] : v[j + 1];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float g = upper ? recv : v[j];
-            const float u = upper ? v[j + 1] : recv;
-            const int col = c + j + (upper ? 1 : 0);
-            const float a = g / (1.0f + __expf(-g)) * u;
-            if (col < tl.ntok) out[(size_t)(tl.row0 + col) * ld + i] = __float2bfloat16_rn(a);
+            for (int j = 0; j < 16; ++j)
+              if (c + j < tl.ntok)
+                out[(size_t)(tl.row0 + c + j) * ld + i] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
           }
         }
       } else {
         __nv_bfloat16 *out = tl.shared ? p.out_s : p.out;
-        const int h = tl.rb * 128 + 32 * q + lane;
+        const int ha = tl.rb * 256 + r, hb = ha + 128;
         for (int c = 0; c < tl.N; c += 16) {
-          float v[16];
-          tmem_ld16(taddr + (uint32_t)c, v);
+          float va[16], vb[16];
+          tmem_ld16(t0 + (uint32_t)c, va);
+          tmem_ld16(t0 + (uint32_t)(BN + c), vb);
           tmem_wait_ld();
-          if (h < p.H) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c + j < tl.ntok) out[(size_t)(tl.row0 + c + j) * p.H + h] = __float2bfloat16_rn(v[j]);
+          for (int j = 0; j < 16; ++j) {
+            if (c + j < tl.ntok) {
+              __nv_bfloat16 *row = out + (size_t)(tl.row0 + c + j) * p.H;
+              if (ha < p.H) row[ha] = __float2bfloat16_rn(va[j]);
+              if (hb < p.H) row[hb] = __float2bfloat16_rn(vb[j]);
+            }
           }
         }
       }
@@ -397,9 +440,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
 
   __syncwarp();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, L::kTmemCols);
   }
 }
 

@@ -12,22 +12,27 @@ namespace moe {
 
 // ---------------------------------------------------------------- router
 struct RouterParams {
-  CUtensorMap map_x;  // hidden [T][H] bf16, box {64, 128}, 128-byte swizzle
-  CUtensorMap map_w;  // router_w [E][H] fp32, box {64, Epad}, no swizzle (rows >= E read as zero)
-  const float *bias;  // [E] or nullptr
-  float *logits_out;  // [T][E] or nullptr
-  unsigned *err;      // workspace error word or nullptr
-  int32_t *topk_idx;  // [T][k]
-  float *topk_w;      // [T][k]
+  CUtensorMap map_x;         // hidden [T][H] bf16, box {64, 128}, 128-byte swizzle
+  CUtensorMap map_hi;        // W_high [E][H] bf16 (workspace), box {64, Epad}, 128-byte swizzle (rows >= E read 0)
+  CUtensorMap map_lo;        // W_low, as map_hi
+  __nv_bfloat16 *w_hi, *w_lo;  // [E][H] each, written by the split kernel
+  float *partial;            // [KS][T][E] partial logits of the H slices
+  const float *bias;         // [E] or nullptr
+  float *logits_out;         // [T][E] or nullptr
+  unsigned *err;             // workspace error word or nullptr
+  int32_t *topk_idx;         // [T][k]
+  float *topk_w;             // [T][k]
   int T, H, E, Epad, top_k, score_mode;
   float route_scale, renorm_eps;
-  int kslices_per_cta;  // 64-wide K slices handled by one CTA of a cluster
+  int kslices_per_cta;       // 64-wide K slices handled by one CTA
   int stages;
 };
-constexpr int kRouterThreads = 192;  // warps 0-3 convert + epilogue, 4 MMA, 5 TMA
+constexpr int kRouterThreads = 192;  // warp 0 TMA, 1 MMA, 2-5 epilogue
 size_t router_smem_bytes(int Epad, int stages);
 int router_stages(int Epad);
-cudaError_t launch_router(const RouterParams &p, int ksplit, int mtiles, cudaStream_t stream, bool pdl);
+// split (router_w -> w_hi, w_lo), gemm (grid ksplit x mtiles), topk (grid T)
+cudaError_t launch_router(const RouterParams &p, const float *router_w, int ksplit, int mtiles, cudaStream_t stream,
+                          bool pdl);
 
 // --------------------------------------------------------------- permute
 struct PermuteParams {
@@ -44,12 +49,13 @@ cudaError_t launch_permute(const PermuteParams &p, cudaStream_t stream, bool pdl
 // ------------------------------------------------------- grouped expert GEMM
 enum GemmMode { kGateUp = 0, kDown = 1 };
 struct GemmParams {
-  CUtensorMap map_a0;  // gate/up: w_gate {H, I, E} box {64,16,1}; down: w_down {I, H, E} box {64,128,1}
-  CUtensorMap map_a1;  // gate/up: w_up (as map_a0); down: unused
-  CUtensorMap map_s0;  // gate/up: ws_gate {H, Is} box {64,16}; down: ws_down {Is, H} box {64,128}
-  CUtensorMap map_s1;  // gate/up: ws_up; down: unused
-  CUtensorMap map_b;   // gate/up: hidden {H, T} box {64,1} (gather4); down: A_act {I, S} box {64,16}
-  CUtensorMap map_bs;  // down: A_shared {Is, T} box {64,16}; gate/up: unused
+  CUtensorMap map_a0;     // gate/up: w_gate {H, I, E} box {64,128,1}; down: w_down {I, H, E} box {64,128,1}
+  CUtensorMap map_a1;     // gate/up: w_up (as map_a0); down: unused
+  CUtensorMap map_s0;     // gate/up: ws_gate {H, Is} box {64,128}; down: ws_down {Is, H} box {64,128}
+  CUtensorMap map_s1;     // gate/up: ws_up; down: unused
+  CUtensorMap map_b[4];   // down: A_act {I, S}, boxes {64, 16/32/64/128}; gate/up: unused
+  CUtensorMap map_bs[4];  // down: A_shared {Is, T}, boxes {64, 16/32/64/128}; gate/up: unused
+  const __nv_bfloat16 *hidden;  // gate/up: [T][H], read row by row through perm
   const int32_t *perm;
   const int32_t *offsets;
   __nv_bfloat16 *out;    // gate/up: A_act [S][I]; down: y_sorted [S][H]
@@ -57,8 +63,8 @@ struct GemmParams {
   unsigned *err;
   int T, H, E, I, Is, top_k, S, has_shared;
 };
-constexpr int kGemmThreads = 192;
-int gemm_tile_n(int T);  // tokens per tile (multiple of 16) chosen for a T
+constexpr int kGemmThreads = 288;  // warps 0-3 producers, 4 MMA, 5-8 epilogue
+int gemm_tile_n(int T);            // tokens per tile (multiple of 16, <= 256) chosen for a T
 cudaError_t launch_expert_gemm(const GemmParams &p, GemmMode mode, int bn, int num_ctas, cudaStream_t stream,
                                bool pdl);
 

@@ -1,5 +1,5 @@
-// Inline-PTX building blocks for sm_103a: mbarriers, TMA (tiled, gather4,
-// bulk store), tcgen05 (TMEM alloc, MMA, commit, loads), programmatic
+// Inline-PTX building blocks for sm_103a: mbarriers, TMA (tiled loads),
+// tcgen05 (TMEM alloc, MMA, commit, loads), programmatic
 // dependent launch, and waits bounded by %globaltimer.
 #pragma once
 #include <cuda.h>
@@ -92,16 +92,6 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
       "%4, %5}], [%2], %6;" ::"r"(dst),
       "l"(m), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
-}
-// Four rows r0..r3 (each one box of the map's inner width) into 4 consecutive
-// smem rows.  The map's box is one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int r0, int r1,
-                                            int r2, int r3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
-      "l"(m), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {

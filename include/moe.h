@@ -114,15 +114,15 @@ moe_status moe_ws_read_error(void *ws, size_t ws_bytes, int clear, void *stream,
 /* Steps a1-a2: router GEMM and routing.  [case] section 2; [hy3] MoE routing;
  * [image] easy_topk.
  *   hidden      [T, H] bf16 row-major (input)
- *   router_w    [E, H] fp32 row-major (input); the kernel forms
- *               W_high = bf16_RNE(W), W_low = bf16_RNE((W - W_high) * 256) on the
- *               fly, runs two BF16 tensor-core GEMMs into two fp32 accumulators
- *               and takes logits = acc_lo * (1/256) + acc_hi in one FFMA
+ *   router_w    [E, H] fp32 row-major (input); a first pass writes
+ *               W_high = bf16_RNE(W), W_low = bf16_RNE((W - W_high) * 256) into the
+ *               workspace, then two BF16 tensor-core GEMMs run into two fp32
+ *               accumulators and logits = acc_lo * (1/256) + acc_hi (one FFMA);
+ *               the K dimension may be split across CTAs, whose partial logits
+ *               are summed in a fixed order
  *   expert_bias [E] fp32 (input, may be NULL = zeros; sigmoid mode only)
  *   logits_out  [T, E] fp32 (output, may be NULL)
  *   topk_idx    [T, top_k] int32 (output), topk_w [T, top_k] fp32 (output) */
-/* ws may be NULL (this step needs no scratch); when given (>= 256 bytes, 256-byte
- * aligned), device-side anomalies are recorded in its error word. */
 moe_status moe_route(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
                      const float *expert_bias, float *logits_out, int32_t *topk_idx, float *topk_w,
                      void *ws, size_t ws_bytes, void *stream);
@@ -179,7 +179,7 @@ moe_status moe_expert_down(const moe_dims *d, const int32_t *offsets, const moe_
  *   Arguments and results as for moe_expert_ffn (the caller still passes every
  *   input and output).  Dims whose moe_workspace_bytes() exceeds 32 MiB are
  *   rejected with MOE_ERR_WORKSPACE before anything is launched (for the Hy3
- *   shape that admits batches up to about T = 300 tokens).
+ *   shape that admits batches up to T = 241 tokens).
  *   The first call on a device looks up that device's address of the array
  *   (cudaGetSymbolAddress); make that first call before any stream capture.
  *   Every call uses the same array: calls that overlap on the device (two

@@ -78,6 +78,8 @@ def _check_route(w, inp, dl):
         alt = oracle.routing_weights_for(ref["scores"][t:t + 1], np.sort(gi[t:t + 1], 1), w.score_mode,
                                          w.route_scale, w.renorm_eps)[0]
         np.testing.assert_allclose(np.sort(gw[t]), np.sort(alt), atol=2e-4 * max(1.0, w.route_scale))
+    if getattr(dl, "ws", None) is not None:
+        assert moe.moe_ws_read_error(dl.ws) == 0
     # descending key order inside a row (ties: lower expert first)
     k_of = ref["keys"]
     for t in same[:64]:
@@ -98,7 +100,7 @@ def test_route_parity(w):
         dl = type("R", (), {})()
         dl.d = d
         dl.hidden, dl.router_w, dl.bias = bf16_dev(hidden), f32_dev(router_w), f32_dev(bias)
-        dl.ws = None
+        dl.ws = moe.alloc_workspace(d)
         dl.route = lambda: DeviceLayer.route(dl)
     else:
         dl = DeviceLayer(w, inp)
@@ -114,9 +116,10 @@ def test_route_parity_full_size(name, T):
     dl = type("R", (), {})()
     dl.d = dims_of(w)
     dl.hidden, dl.router_w, dl.bias = bf16_dev(hidden), f32_dev(router_w), f32_dev(bias)
-    dl.ws = None
+    dl.ws = moe.alloc_workspace(dl.d)
     dl.route = lambda: DeviceLayer.route(dl)
     gi, ref, ties = _check_route(w, inp, dl)
+    assert moe.moe_ws_read_error(dl.ws) == 0
     print(f"{name}: near-tie rows where the GPU chose differently: {len(ties)}; "
           f"rows with margin < 1e-5: {int((ref['margin'] < NEAR_TIE).sum())}")
 
@@ -198,9 +201,11 @@ def test_expert_ffn_parity(w):
     assert moe.moe_ws_read_error(dl.ws) == 0
 
 
-def test_expert_ffn_skewed_segments():
-    """One expert holding every token (several 256-token chunks) and empty experts."""
-    w = MID.with_(name="mid_skew", T=700)
+@pytest.mark.parametrize("T", [700, 512])
+def test_expert_ffn_skewed_segments(T):
+    """One expert holding every token (several chunks; T = 512 gives chunks of exactly
+    256 tokens, the widest tile) and empty experts."""
+    w = MID.with_(name="mid_skew", T=T)
     inp = W.layer_inputs(w)
     topk = np.zeros((w.T, 2), dtype=np.int32)
     topk[:, 0] = 3
