@@ -55,11 +55,18 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_hash() -> str:
-    """Hash of the CUDA sources: stored ncu counters are used only for the same kernels."""
+KERNEL_SOURCES = {  # the files that define each kernel's code
+    "gate_up": ["expert_gemm.cu", "ptx.cuh"], "down": ["expert_gemm.cu", "ptx.cuh"],
+    "route": ["router.cu", "ptx.cuh"], "permute": ["permute.cu", "ptx.cuh"], "combine": ["combine.cu", "ptx.cuh"],
+}
+
+
+def source_hash(kernel: str) -> str:
+    """Hash of a kernel's sources: stored ncu counters are used only for the same code."""
     h = hashlib.sha256()
-    for f in sorted((ROOT / "expert_ffn_layer_gb300" / "csrc").glob("*")):
-        h.update(f.name.encode())
+    for name in KERNEL_SOURCES[kernel]:
+        f = ROOT / "expert_ffn_layer_gb300" / "csrc" / name
+        h.update(name.encode())
         h.update(f.read_bytes())
     return h.hexdigest()[:16]
 
@@ -70,10 +77,10 @@ def stored_traffic(kernel: str, workload: str):
     if not p.exists():
         return None
     d = json.loads(p.read_text())
-    if d.get("source_hash") != source_hash():
-        return None
     k = d.get("kernels", {}).get(kernel)
-    return None if k is None else float(k["dram_bytes_per_launch"])
+    if k is None or k.get("source_hash") != source_hash(kernel):
+        return None
+    return float(k["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -126,6 +133,34 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- multi-rank helpers
+
+def replica_hidden(w, rank: int):
+    """Tokens of one replica: rank 0 uses the workload's own hidden states (so a
+    one-GPU run is the workload itself); rank r > 0 draws its own seeded batch."""
+    import workloads as W
+
+    if rank == 0:
+        return W.router_inputs(w)[0]
+    return W.normal_bf16(w.seed + 1000 * rank, W.TID_HIDDEN, (w.T, w.H), w.hidden_sigma)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The slowest rank's time (all ranks get the same value)."""
+    if world == 1:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step: int, steps: int, total_ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch each step (weak scaling)."""
+    return world * tokens_per_step * steps / (total_ms * 1e-3)
 
 
 # ----------------------------------------------------------------------------- algorithmic work
@@ -195,9 +230,8 @@ def run_ours(args, rank, world, local_rank):
     def setup(name, replica_seed):
         w = W.WORKLOADS[name]
         t0 = time.time()
-        hidden_np, router_w, bias = W.router_inputs(w)
-        if replica_seed:  # each rank of a weak-scaling run has its own tokens, same weights
-            hidden_np = W.normal_bf16(w.seed + 1000 * replica_seed, W.TID_HIDDEN, (w.T, w.H), w.hidden_sigma)
+        _, router_w, bias = W.router_inputs(w)
+        hidden_np = replica_hidden(w, replica_seed)  # each rank has its own tokens, same weights
         gate, up, down = W.expert_weights(w)
         sg, su, sd = W.shared_weights(w)
         d = moe.dims(w.T, w.H, w.E, w.I, w.top_k, w.I_shared, w.score_mode, w.route_scale, w.renorm_eps,
@@ -220,13 +254,6 @@ def run_ours(args, rank, world, local_rank):
             ev[i][1].record()
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in ev]
-
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
 
     def graph_of(fn, reps):
         """A CUDA graph of `reps` back-to-back calls (no host gaps between kernels)."""
@@ -313,12 +340,12 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = max_over_ranks(float(np.sum(per_step)))
+    total_ms = max_over_ranks(float(np.sum(per_step)), world, dev)
     err = moe.moe_ws_read_error(layer.ws)
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed steps")
-    value = world * w.T * args.steps / (total_ms * 1e-3)
-    eager_ms = max_over_ranks(float(np.sum(timed(eager_step, args.steps, 1))))
+    value = job_throughput(world, w.T, args.steps, total_ms)
+    eager_ms = max_over_ranks(float(np.sum(timed(eager_step, args.steps, 1))), world, dev)
 
     # ---------------- end to end through MoELayer with host buffers
     h_in = torch.from_numpy(np.ascontiguousarray(hidden_np).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -329,8 +356,8 @@ def run_ours(args, rank, world, local_rank):
         layer(hidden, out)
         h_out.copy_(out, non_blocking=True)
 
-    e2e_ms = max_over_ranks(float(np.sum(timed(e2e_step, args.steps, max(1, args.warmup)))))
-    e2e_value = world * w.T * args.steps / (e2e_ms * 1e-3)
+    e2e_ms = max_over_ranks(float(np.sum(timed(e2e_step, args.steps, max(1, args.warmup)))), world, dev)
+    e2e_value = job_throughput(world, w.T, args.steps, e2e_ms)
 
     # ---------------- per-kernel durations -> roofline of the dominant kernel
     st_ms, n_active, counts = stage_times(w, d, layer, hidden, args.steps)

@@ -31,7 +31,7 @@ SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
 
 EXPORTS = ("moe_status_string", "moe_check_dims", "moe_workspace_bytes", "moe_ws_init", "moe_ws_read_error",
            "moe_route", "moe_permute", "moe_expert_ffn", "moe_expert_gate_up", "moe_expert_down", "moe_combine",
-           "moe_layer_forward", "moe_expert_ffn_noalloc")
+           "moe_layer_forward", "moe_expert_ffn_noalloc", "moe_selftest_wait_timeout")
 
 
 class MoeError(RuntimeError):
@@ -81,6 +81,7 @@ def load() -> ctypes.CDLL:
         "moe_expert_down": (st, [D, P, P, P, P, P, P, C, P]),
         "moe_combine": (st, [D, P, P, P, P, P, P]),
         "moe_layer_forward": (st, [D, P, P, P, P, P, P, P, P, P, P, P, C, P]),
+        "moe_selftest_wait_timeout": (st, [P, C, ctypes.c_ulonglong, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -240,6 +241,10 @@ def moe_layer_forward(d: MoeDims, hidden, router_w, expert_bias, w_gate, w_up, w
     _call("moe_layer_forward", ctypes.byref(d), _ptr(hidden), _ptr(router_w), _ptr(expert_bias), _ptr(w_gate),
           _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(out), _ptr(ws), ws.numel(),
           _stream(stream))
+
+
+def moe_selftest_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> None:
+    _call("moe_selftest_wait_timeout", _ptr(ws), ws.numel(), limit_ns, _stream(stream))
 
 
 class MoELayer:

@@ -339,6 +339,12 @@ MOE_API moe_status moe_ws_read_error(void *ws, size_t ws_bytes, int clear, void 
   return MOE_OK;
 }
 
+MOE_API moe_status moe_selftest_wait_timeout(void *ws, size_t ws_bytes, unsigned long long limit_ns, void *stream) {
+  if (ws == nullptr || !aligned256(ws) || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_timeout(at<unsigned>(ws, 0), limit_ns, (cudaStream_t)stream));
+}
+
 MOE_API moe_status moe_route(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
                              const float *expert_bias, float *logits_out, int32_t *topk_idx, float *topk_w, void *ws,
                              size_t ws_bytes, void *stream) {

@@ -79,6 +79,9 @@ struct CombineParams {
 };
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream, bool pdl);
 
+// self-test: a bounded wait on a barrier nothing completes (records MOE_DEVERR_TIMEOUT)
+cudaError_t launch_wait_timeout(unsigned *err, unsigned long long limit_ns, cudaStream_t stream);
+
 // shared launch helper: PDL attribute on, optional cluster dims
 cudaError_t launch_ex(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
                       int cluster_x, void **args);

@@ -48,23 +48,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `parity` to complete.  Returns false (after recording
-// the timeout in *err and in *abort) if it has not completed within the limit,
+// the timeout in *err and in *abort) if it has not completed within limit_ns,
 // or early if another role of the block has already given up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err,
-                                          volatile int *abort_flag) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned *err, volatile int *abort_flag,
+                                              unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         if (err != nullptr) atomicOr(err, MOE_DEVERR_TIMEOUT);
         if (abort_flag != nullptr) *abort_flag = 1;
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err, volatile int *abort_flag) {
+  return mbar_wait_for(bar, parity, err, abort_flag, kWaitLimitNs);
 }
 
 // ------------------------------------------------------------------- TMA

@@ -111,6 +111,13 @@ moe_status moe_ws_init(void *ws, size_t ws_bytes, void *stream);
  * call that synchronises `stream`; *bits receives MOE_DEVERR_* flags. */
 moe_status moe_ws_read_error(void *ws, size_t ws_bytes, int clear, void *stream, uint32_t *bits);
 
+/* Self-test of the bounded waits inside the kernels: one CTA waits on a
+ * barrier phase that nothing completes, gives up after limit_ns (1 ns .. 10 s),
+ * records MOE_DEVERR_TIMEOUT in the workspace error word and returns; read it
+ * with moe_ws_read_error.  Every wait in this library's kernels is bounded the
+ * same way (1 s), so a broken pipeline reports an error instead of hanging. */
+moe_status moe_selftest_wait_timeout(void *ws, size_t ws_bytes, unsigned long long limit_ns, void *stream);
+
 /* Steps a1-a2: router GEMM and routing.  [case] section 2; [hy3] MoE routing;
  * [image] easy_topk.
  *   hidden      [T, H] bf16 row-major (input)

@@ -355,3 +355,22 @@ def test_layer_full_size_sampled(name):
     print(f"{name}: sampled rows {len(rows)} rel_l2={r:.3e} max_abs={m:.3e} near-tie rows={nties}; "
           f"expert counts max={c.max()} min={c.min()} empty={(c == 0).sum()}")
     assert moe.moe_ws_read_error(dl.ws) == 0
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A kernel wait that nothing completes gives up after its limit, records
+    MOE_DEVERR_TIMEOUT, and the GPU keeps working: a layer forward afterwards
+    still matches the oracle."""
+    w = W.WORKLOADS["tiny"]
+    d = dims_of(w)
+    ws = moe.alloc_workspace(d)
+    moe.moe_selftest_wait_timeout(ws, 20_000_000)  # 20 ms
+    bits = moe.moe_ws_read_error(ws, clear=True)
+    assert bits & moe.DEVERR_TIMEOUT
+    assert moe.moe_ws_read_error(ws) == 0
+    inp = inputs_of(w)
+    dl = DeviceLayer(w, inp)
+    out = dl.forward()
+    idx, _, _ = dl.route()
+    torch.cuda.synchronize()
+    _check_layer_rows(w, inp, host_f64(out), np.arange(w.T), idx.cpu().numpy())
