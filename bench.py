@@ -56,6 +56,7 @@ def peaks():
 
 
 KERNEL_SOURCES = {  # the files that define each kernel's code
+    "expert_ffn": ["expert_gemm.cu", "ptx.cuh"],
     "gate_up": ["expert_gemm.cu", "ptx.cuh"], "down": ["expert_gemm.cu", "ptx.cuh"],
     "route": ["router.cu", "ptx.cuh"], "permute": ["permute.cu", "ptx.cuh"], "combine": ["combine.cu", "ptx.cuh"],
 }
@@ -181,6 +182,12 @@ def stage_work(w, n_active: int):
         "down": {"bytes": (n_active * I + ns * Is) * H * 2 + (S * I + Ts * Is) * 2 + (S + Ts) * H * 2,
                  "flops": 2 * (S * H * I + Ts * H * Is)},
         "combine": {"bytes": S * H * 2 + Ts * H * 2 + T * H * 2 + S * 8, "flops": 2 * S * H},
+        # the fused persistent kernel (gate/up then down, one launch): every activated
+        # expert's three weight matrices, token rows in, expert outputs out, and the
+        # bf16 activations written and read back
+        "expert_ffn": {"bytes": (n_active * 3 * I + ns * 3 * Is) * H * 2 + (S + Ts) * H * 2 + (S + Ts) * H * 2
+                                + 2 * (S * I + Ts * Is) * 2,
+                       "flops": 6 * (S * H * I + Ts * H * Is)},
     }
 
 
@@ -287,9 +294,12 @@ def run_ours(args, rank, world, local_rank):
         calls = {
             "route": lambda: moe.moe_route(d, hidden, L.router_w, L.expert_bias, idx, wts, ws),
             "permute": lambda: moe.moe_permute(d, idx, counts, offs, perm, inv, ws),
+            "expert_ffn": lambda: moe.moe_expert_ffn(d, hidden, perm, offs, L.w_gate, L.w_up, L.w_down, L.ws_gate,
+                                                     L.ws_up, L.ws_down, y, z, ws),
+            "combine": lambda: moe.moe_combine(d, y, z, inv, wts, out),
+            # the two phases of expert_ffn as separate launches, for reference
             "gate_up": lambda: moe.moe_expert_gate_up(d, hidden, perm, offs, L.w_gate, L.w_up, L.ws_gate, L.ws_up, ws),
             "down": lambda: moe.moe_expert_down(d, offs, L.w_down, L.ws_down, y, z, ws),
-            "combine": lambda: moe.moe_combine(d, y, z, inv, wts, out),
         }
         for name in calls:  # produce every intermediate once, in order
             calls[name]()
@@ -362,7 +372,8 @@ def run_ours(args, rank, world, local_rank):
     # ---------------- per-kernel durations -> roofline of the dominant kernel
     st_ms, n_active, counts = stage_times(w, d, layer, hidden, args.steps)
     work = stage_work(w, n_active)
-    dominant = max(st_ms, key=st_ms.get)
+    in_layer = ("route", "permute", "expert_ffn", "combine")
+    dominant = max(in_layer, key=st_ms.get)
     roof = roofline_for(dominant, work, st_ms[dominant], pk, pk_kind, f"{name}_T{w.T}", bound="hbm")
     kernels = {n: {"ms": round(v, 4), **{kk: vv for kk, vv in roofline_for(n, work, v, pk, pk_kind,
                                                                             f"{name}_T{w.T}").items()
@@ -377,12 +388,12 @@ def run_ours(args, rank, world, local_rank):
                 "N(0,0.1) expert bias (the pages' shapes; no trained weights)",
         "config": {**w.describe(), "workload": f"hy3_{name}_T{w.T}", "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "CUDA graph of one layer forward (7 kernels, PDL-chained)",
+                   "launch": "CUDA graph of one layer forward (6 kernels, PDL-chained)",
                    "eager_ms_per_step": round(eager_ms / args.steps, 5),
                    "active_experts": n_active, "max_tokens_per_expert": int(counts.max())},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": w.T * w.H * 2,
                 "d2h_bytes_per_step": w.T * w.H * 2, "ms_per_step": round(e2e_ms / args.steps, 5)},
-        "gpu_launches": 7 * args.steps,  # split, router gemm, top-k, permute, gate/up, down, combine
+        "gpu_launches": 6 * args.steps,  # split, router gemm, top-k, permute, expert FFN, combine
         "roofline": roof,
         "kernels": kernels,
         "clocks": clk.summary(),
@@ -399,9 +410,9 @@ def run_ours(args, rank, world, local_rank):
         pms = float(np.mean(pst))
         pst_ms, pact, pcounts = stage_times(pw, pd, player, phidden, max(3, args.steps // 2))
         pwork = stage_work(pw, pact)
-        flops = sum(v["flops"] for k, v in pwork.items() if k in ("gate_up", "down"))
-        wbytes = sum(pwork[k]["bytes"] for k in ("gate_up", "down"))
-        pdom = max(pst_ms, key=pst_ms.get)
+        flops = pwork["expert_ffn"]["flops"]
+        wbytes = (pact * 3 * pw.I + 3 * pw.I_shared) * pw.H * 2
+        pdom = max(("route", "permute", "expert_ffn", "combine"), key=pst_ms.get)
         result["prefill"] = {
             "workload": f"hy3_prefill_T{pw.T}", "value": round(pw.T / (pms * 1e-3), 1), "unit": UNIT,
             "ms_per_step": round(pms, 5), "active_experts": pact, "max_tokens_per_expert": int(pcounts.max()),
@@ -409,7 +420,7 @@ def run_ours(args, rank, world, local_rank):
             "layer_hbm_frac": round(wbytes / (pms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
             "roofline": roofline_for(pdom, pwork, pst_ms[pdom], pk, pk_kind, f"prefill_T{pw.T}"),
             "kernels": {n: round(v, 4) for n, v in pst_ms.items()},
-            "gpu_launches": 7 * args.steps,  # split, router gemm, top-k, permute, gate/up, down, combine
+            "gpu_launches": 6 * args.steps,  # split, router gemm, top-k, permute, expert FFN, combine
         }
         del player, phidden, pgraph
         torch.cuda.empty_cache()

@@ -115,7 +115,7 @@ WsLayout ws_layout(const moe_dims &d) {
   };
   const size_t T = (size_t)d.T, S = (size_t)d.T * d.top_k, E = (size_t)d.E;
   const size_t Is = d.has_shared ? (size_t)d.I_shared : 0;
-  L.err = take(256);
+  L.err = take(kWsHeaderBytes);  // error word + tile-scheduler counters
   L.topk_idx = take(S * 4);
   L.topk_w = take(S * 4);
   L.counts = take(E * 4);
@@ -205,13 +205,16 @@ moe_status do_permute(const moe_dims &d, const int32_t *topk_idx, int32_t *count
   return cuda_status(launch_permute(p, stream, pdl));
 }
 
-GemmParams gemm_common(const moe_dims &d, const int32_t *perm, const int32_t *offsets, void *ws) {
+// Tensor maps and pointers of the grouped expert FFN; `phases` selects gate/up
+// (1), down (2) or both in one persistent launch (3).
+moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidden, const int32_t *perm,
+                            const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                            const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
+                            const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws,
+                            cudaStream_t stream, bool pdl) {
   const WsLayout L = ws_layout(d);
   GemmParams g;
   std::memset(&g, 0, sizeof(g));
-  g.perm = perm;
-  g.offsets = offsets;
-  g.err = at<unsigned>(ws, L.err);
   g.T = d.T;
   g.H = d.H;
   g.E = d.E;
@@ -220,50 +223,56 @@ GemmParams gemm_common(const moe_dims &d, const int32_t *perm, const int32_t *of
   g.top_k = d.top_k;
   g.S = d.T * d.top_k;
   g.has_shared = d.has_shared;
-  return g;
+  g.phases = phases;
+  g.hidden = reinterpret_cast<const __nv_bfloat16 *>(hidden);
+  g.perm = perm;
+  g.offsets = offsets;
+  g.err = at<unsigned>(ws, L.err);
+  g.sync = at<unsigned>(ws, L.err);
+  g.act = at<__nv_bfloat16>(ws, L.a_act);
+  g.act_s = at<__nv_bfloat16>(ws, L.a_shared);
+  g.y = reinterpret_cast<__nv_bfloat16 *>(y_sorted);
+  g.y_s = reinterpret_cast<__nv_bfloat16 *>(y_shared);
+  bool ok = true;
+  if (phases & 1) {
+    ok = ok && map_bf16_3d(&g.map_wg, w_gate, d.H, d.I, d.E, 128) && map_bf16_3d(&g.map_wu, w_up, d.H, d.I, d.E, 128);
+    if (d.has_shared)
+      ok = ok && map_bf16_2d(&g.map_sg, ws_gate, d.H, g.Is, 128) && map_bf16_2d(&g.map_su, ws_up, d.H, g.Is, 128);
+  }
+  if (phases & 2) {
+    ok = ok && map_bf16_3d(&g.map_wd, w_down, d.I, d.H, d.E, 128);
+    for (int b = 0; b < 4; ++b) ok = ok && map_bf16_2d(&g.map_act[b], g.act, d.I, g.S, 16u << b);
+    if (d.has_shared) {
+      ok = ok && map_bf16_2d(&g.map_sd, ws_down, g.Is, d.H, 128);
+      for (int b = 0; b < 4; ++b) ok = ok && map_bf16_2d(&g.map_acts[b], g.act_s, g.Is, d.T, 16u << b);
+    }
+  }
+  if (!ok) return MOE_ERR_CUDA;
+  return cuda_status(launch_expert_ffn(g, gemm_tile_n(d.T), num_sms(), stream, pdl));
 }
 
 // a5-a6: gate/up GEMM through the route index + SiLU(gate) * up -> activations in ws
 moe_status do_gate_up(const moe_dims &d, const moe_bf16 *hidden, const int32_t *perm, const int32_t *offsets,
                       const moe_bf16 *w_gate, const moe_bf16 *w_up, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
                       void *ws, cudaStream_t stream, bool pdl) {
-  const WsLayout L = ws_layout(d);
-  GemmParams g = gemm_common(d, perm, offsets, ws);
-  bool ok = map_bf16_3d(&g.map_a0, w_gate, d.H, d.I, d.E, 128) && map_bf16_3d(&g.map_a1, w_up, d.H, d.I, d.E, 128);
-  if (d.has_shared)
-    ok = ok && map_bf16_2d(&g.map_s0, ws_gate, d.H, g.Is, 128) && map_bf16_2d(&g.map_s1, ws_up, d.H, g.Is, 128);
-  if (!ok) return MOE_ERR_CUDA;
-  g.hidden = reinterpret_cast<const __nv_bfloat16 *>(hidden);
-  g.out = at<__nv_bfloat16>(ws, L.a_act);
-  g.out_s = at<__nv_bfloat16>(ws, L.a_shared);
-  return cuda_status(launch_expert_gemm(g, kGateUp, gemm_tile_n(d.T), num_sms(), stream, pdl));
+  return do_expert_phases(d, 1, hidden, perm, offsets, w_gate, w_up, nullptr, ws_gate, ws_up, nullptr, nullptr,
+                          nullptr, ws, stream, pdl);
 }
 
 // a7-a8: down GEMM over the activations in ws -> y_sorted, y_shared
 moe_status do_down(const moe_dims &d, const int32_t *offsets, const moe_bf16 *w_down, const moe_bf16 *ws_down,
                    moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl) {
-  const WsLayout L = ws_layout(d);
-  GemmParams h = gemm_common(d, nullptr, offsets, ws);
-  bool ok = map_bf16_3d(&h.map_a0, w_down, d.I, d.H, d.E, 128);
-  for (int b = 0; b < 4; ++b) ok = ok && map_bf16_2d(&h.map_b[b], at<moe_bf16>(ws, L.a_act), d.I, h.S, 16u << b);
-  if (d.has_shared) {
-    ok = ok && map_bf16_2d(&h.map_s0, ws_down, h.Is, d.H, 128);
-    for (int b = 0; b < 4; ++b)
-      ok = ok && map_bf16_2d(&h.map_bs[b], at<moe_bf16>(ws, L.a_shared), h.Is, d.T, 16u << b);
-  }
-  if (!ok) return MOE_ERR_CUDA;
-  h.out = reinterpret_cast<__nv_bfloat16 *>(y_sorted);
-  h.out_s = reinterpret_cast<__nv_bfloat16 *>(y_shared);
-  return cuda_status(launch_expert_gemm(h, kDown, gemm_tile_n(d.T), num_sms(), stream, pdl));
+  return do_expert_phases(d, 2, nullptr, nullptr, offsets, nullptr, nullptr, w_down, nullptr, nullptr, ws_down,
+                          y_sorted, y_shared, ws, stream, pdl);
 }
 
+// a5-a8 in one persistent launch
 moe_status do_expert_ffn(const moe_dims &d, const moe_bf16 *hidden, const int32_t *perm, const int32_t *offsets,
                          const moe_bf16 *w_gate, const moe_bf16 *w_up, const moe_bf16 *w_down,
                          const moe_bf16 *ws_gate, const moe_bf16 *ws_up, const moe_bf16 *ws_down, moe_bf16 *y_sorted,
                          moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl) {
-  moe_status st = do_gate_up(d, hidden, perm, offsets, w_gate, w_up, ws_gate, ws_up, ws, stream, pdl);
-  if (st != MOE_OK) return st;
-  return do_down(d, offsets, w_down, ws_down, y_sorted, y_shared, ws, stream, true);
+  return do_expert_phases(d, 3, hidden, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_sorted,
+                          y_shared, ws, stream, pdl);
 }
 
 moe_status do_combine(const moe_dims &d, const moe_bf16 *y_sorted, const moe_bf16 *y_shared, const int32_t *inv,
@@ -323,8 +332,8 @@ MOE_API size_t moe_workspace_bytes(const moe_dims *d) {
 }
 
 MOE_API moe_status moe_ws_init(void *ws, size_t ws_bytes, void *stream) {
-  if (ws == nullptr || !aligned256(ws) || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
-  return cuda_status(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream));
+  if (ws == nullptr || !aligned256(ws) || ws_bytes < (size_t)kWsHeaderBytes) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, kWsHeaderBytes, (cudaStream_t)stream));
 }
 
 MOE_API moe_status moe_ws_read_error(void *ws, size_t ws_bytes, int clear, void *stream, uint32_t *bits) {
@@ -514,8 +523,9 @@ MOE_API moe_status moe_expert_ffn_noalloc(const moe_dims *d, const moe_bf16 *hid
   void *ws = static_scratch(&e);
   if (ws == nullptr) return MOE_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
-  // the array keeps the previous call's contents: the header (error word) must start at zero
-  if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the array keeps the previous call's contents: the header (error word and
+  // tile-scheduler counters) must start at zero
+  if (cudaMemsetAsync(ws, 0, kWsHeaderBytes, s) != cudaSuccess) return MOE_ERR_CUDA;
   return do_expert_ffn(*d, hidden, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_sorted, y_shared,
                        ws, s, true);
 }

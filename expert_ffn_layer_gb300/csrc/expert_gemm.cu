@@ -1,5 +1,7 @@
-// Steps a5-a8: grouped expert GEMMs over uneven expert segments (plus the
-// shared expert as one more segment), on the 5th-generation tensor cores.
+// Steps a5-a8: the grouped expert FFN -- gate/up GEMM through the route index,
+// SiLU(gate) * up, down GEMM -- over uneven expert segments plus the shared
+// expert as one more segment, in one persistent kernel on the 5th-generation
+// tensor cores.
 //
 // "Hy3 Preview inference optimisation case", section 3 (FusedMoE): the gate-up
 // GEMM reads the original input through the route index (no explicit gather
@@ -7,30 +9,36 @@
 // SwiGLU experts down(SiLU(gate(x)) * up(x)), stacked expert weights, the
 // shared MLP applied to every token.
 //
-// Orientation: weight rows are the M = 128 operand of every MMA and the tokens
-// of one expert chunk are the N operand (N = tokens rounded up to 16, at most
+// Tiles.  Weight rows are the M = 128 operand of every MMA and the tokens of
+// one expert chunk are the N operand (N = tokens rounded up to 16, at most
 // BN <= 256).  A tile is 256 weight rows x N tokens: two MMAs per K step share
 // one token tile and accumulate into two TMEM accumulators,
-//   gate/up: D0 = gate rows i0..i0+127, D1 = up rows i0..i0+127, so gate row i
-//            and up row i land in the same TMEM lane and one thread forms
-//            SiLU(gate) * up -> bf16 activation A_act[p][i];
-//   down:    D0 = w_down rows h0..h0+127, D1 = rows h0+128..h0+255 -> y[p][h].
-// Sharing the token tile between 256 weight rows halves the token re-reads
-// from L2 compared with one 128-row MMA per tile.
+//   gate/up tile: D0 = gate rows i0..i0+127, D1 = up rows i0..i0+127, so gate
+//                 row i and up row i land in the same TMEM lane and one thread
+//                 forms SiLU(gate) * up -> bf16 activation A_act[p][i];
+//   down tile:    D0 = w_down rows h0..h0+127, D1 = rows h0+128..h0+255 ->
+//                 y[p][h].
+// Sharing the token tile between 256 weight rows halves the token re-reads.
 //
 // Operand loads per 64-wide K step: the two 128-row weight boxes by TMA
-// (128-byte swizzle); the token rows of gate/up through the route index
+// (128-byte swizzle); the token rows of a gate/up tile through the route index
 // (token = perm[p] / k) by cp.async from 128 producer threads straight from
-// `hidden`, written in the same swizzled layout (TMA's row-gather moves 4 rows
-// per instruction and tops out far below the rate these tiles need); the
-// activation rows of down, which are contiguous, by at most four TMA boxes.
+// `hidden`, written in the same swizzled layout (TMA's 4-row gather tops out
+// far below the rate these tiles need); the activation rows of a down tile,
+// which are contiguous, by at most four TMA boxes.
 //
-// Persistent CTAs (one per SM) walk the tile list in a static stride; the
-// tile list (per segment: weight row blocks x chunks of <= BN tokens, chunks
-// innermost so chunks of one row block reuse its weights in L2) is derived in
-// every CTA from the expert offsets.  Warp roles: 0-3 producers, 4 MMA issuer
-// (one thread) and TMEM owner, 5-8 epilogue.  A STAGES-deep shared-memory
-// ring overlaps loads and MMAs; for BN <= 128 two TMEM accumulator pairs also
+// Scheduling.  The tile list is every gate/up tile (per segment: 128-row
+// blocks of I x token chunks, chunks innermost so they reuse the block's
+// weights in L2) followed by every down tile.  CTAs (one per SM) claim tiles
+// in that order from an atomic counter, so a down tile is claimed only after
+// every gate/up tile has been claimed by a running CTA: its wait for the
+// gate/up tiles of its segment (a per-segment completion count, bounded) can
+// always be satisfied, whatever the residency of other CTAs.  Gate/up tiles
+// never wait.  The last CTA to leave zeroes the counters for the next call.
+//
+// Warp roles: 0-3 producers (warp 0 lane 0 claims tiles and issues TMA), 4
+// MMA issuer (one thread) and TMEM owner, 5-8 epilogue.  A STAGES-deep ring
+// overlaps loads and MMAs; for BN <= 128 two TMEM accumulator pairs also
 // overlap one tile's epilogue with the next tile's MMAs (BN = 256 fills TMEM
 // with one pair).
 #include "internal.h"
@@ -44,6 +52,7 @@ constexpr int kABytes = 2 * 128 * 128;  // two 128-row x 64-bf16 weight boxes
 constexpr int kMaxSeg = 258;            // E <= 256 routed + 1 shared (+1 sentinel)
 constexpr int kProducers = 128;         // warps 0-3
 constexpr int kMmaWarp = 4;
+constexpr int kRing = 4;                // claimed tile ids in flight
 constexpr unsigned long long kDrainNs = 20000000ull;
 
 template <int BN>
@@ -51,19 +60,20 @@ struct StagesFor {
   static constexpr int value = BN <= 32 ? 6 : BN <= 64 ? 5 : BN <= 128 ? 4 : 3;
 };
 
-template <int MODE, int BN>
+template <int BN>
 struct Layout {
   static constexpr int kStages = StagesFor<BN>::value;
   static constexpr int kStageBytes = kABytes + BN * 128;
   static constexpr int kBarOff = kStages * kStageBytes;
-  static constexpr int kNumBars = 2 * kStages + 5;  // full, empty, tfull[2], tempty[2], drain
-  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
-  static constexpr int kStartOff = kMiscOff + 16;
-  static constexpr int kOffOff = kStartOff + 4 * kMaxSeg;
+  // full, empty per stage; tfull[2], tempty[2]; drain; id_full[kRing], id_empty[kRing]
+  static constexpr int kNumBars = 2 * kStages + 5 + 2 * kRing;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;     // tmem slot, abort flag, ring of tile ids
+  static constexpr int kStart1Off = kMiscOff + 64;
+  static constexpr int kStart2Off = kStart1Off + 4 * kMaxSeg;
+  static constexpr int kOffOff = kStart2Off + 4 * kMaxSeg;
   static constexpr int kBytes = kOffOff + 4 * kMaxSeg;
   static constexpr size_t kSmem = 1024 + kBytes;
-  // accumulator pairs of 2 x BN columns: two (MMA of the next tile overlaps the
-  // epilogue of this one) while they fit in the 512 TMEM columns, else one
+  // accumulator pairs of 2 x BN columns: two while they fit in 512 columns, else one
   static constexpr int kAccBufs = 4 * BN <= 512 ? 2 : 1;
   static constexpr uint32_t kTmemCols = kAccBufs * 2 * BN;
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -71,6 +81,7 @@ struct Layout {
 };
 
 struct Tile {
+  int phase;  // 0 gate/up, 1 down
   int seg, rb, row0, ntok, N, nk, shared;
 };
 
@@ -90,27 +101,33 @@ __device__ __forceinline__ int chunk_count(int cnt) {
 }
 
 // Weight row blocks of a segment: 128 gate/up pairs, or 256 rows of w_down.
-template <int MODE>
-__device__ __forceinline__ int seg_nrb(const GemmParams &p, bool shared) {
-  if (MODE == kGateUp) return ((shared ? p.Is : p.I) + 127) >> 7;
+__device__ __forceinline__ int seg_nrb(const GemmParams &p, int phase, bool shared) {
+  if (phase == 0) return ((shared ? p.Is : p.I) + 127) >> 7;
   return (p.H + 255) >> 8;
 }
 
-template <int MODE, int BN>
-__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const int *tile_start, const int *seg_off,
-                                            int nseg) {
-  int lo = 0, hi = nseg;  // tile_start[nseg] = total > t
+__device__ __forceinline__ int seg_count(const GemmParams &p, const int *seg_off, int s) {
+  return s == p.E ? p.T : seg_off[s + 1] - seg_off[s];
+}
+
+template <int BN>
+__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const int *start1, const int *start2,
+                                            const int *seg_off, int nseg) {
+  Tile tl;
+  tl.phase = t < start1[nseg] ? 0 : 1;
+  const int *ts = tl.phase == 0 ? start1 : start2;
+  const int u = tl.phase == 0 ? t : t - start1[nseg];
+  int lo = 0, hi = nseg;  // ts[nseg] = total of the phase > u
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (tile_start[mid] <= t) lo = mid;
+    if (ts[mid] <= u) lo = mid;
     else hi = mid;
   }
-  Tile tl;
   tl.seg = lo;
   tl.shared = (lo == p.E) ? 1 : 0;
-  const int cnt = tl.shared ? p.T : seg_off[lo + 1] - seg_off[lo];
+  const int cnt = seg_count(p, seg_off, lo);
   const int nch = chunk_count<BN>(cnt);
-  const int local = t - tile_start[lo];
+  const int local = u - ts[lo];
   tl.rb = local / nch;
   const int ch = local - tl.rb * nch;
   const int base = chunk_base<BN>(cnt);
@@ -118,7 +135,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const in
   tl.ntok = min(base, cnt - pin);
   tl.row0 = (tl.shared ? 0 : seg_off[lo]) + pin;
   tl.N = (tl.ntok + 15) & ~15;
-  tl.nk = MODE == kGateUp ? (p.H >> 6) : ((tl.shared ? p.Is : p.I) >> 6);
+  tl.nk = tl.phase == 0 ? (p.H >> 6) : ((tl.shared ? p.Is : p.I) >> 6);
   return tl;
 }
 
@@ -139,20 +156,31 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
 }  // namespace
 
-template <int MODE, int BN>
-__global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using L = Layout<MODE, BN>;
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __grid_constant__ GemmParams p) {
+  using L = Layout<BN>;
   constexpr int STAGES = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = (uint64_t *)(smem + L::kBarOff);
   uint32_t *tmem_slot = (uint32_t *)(smem + L::kMiscOff);
   volatile int *abort_flag = (volatile int *)(smem + L::kMiscOff + 4);
-  int *tile_start = (int *)(smem + L::kStartOff);
+  volatile int *ring = (volatile int *)(smem + L::kMiscOff + 16);  // kRing claimed tile ids
+  int *start1 = (int *)(smem + L::kStart1Off);
+  int *start2 = (int *)(smem + L::kStart2Off);
   int *seg_off = (int *)(smem + L::kOffOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,13 +189,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
   auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
   auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
   const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
+  auto id_full = [&](int r) { return smem_u32(&bars[2 * STAGES + 5 + r]); };
+  auto id_empty = [&](int r) { return smem_u32(&bars[2 * STAGES + 5 + kRing + r]); };
   auto a_smem = [&](int s) { return smem_u32(smem + s * L::kStageBytes); };
   auto b_smem = [&](int s) { return smem_u32(smem + s * L::kStageBytes + kABytes); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // gate/up: 128 cp.async arrivals + the TMA expect_tx arrival; down: TMA only
-      mbar_init(full_bar(s), MODE == kGateUp ? kProducers + 1 : 1);
+      // 128 producer arrivals (cp.async completions or plain) + the TMA expect_tx arrival
+      mbar_init(full_bar(s), kProducers + 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -175,13 +205,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
       mbar_init(tempty_bar(a), 4);
     }
     mbar_init(drain_bar, 1);
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(id_full(r), 1);
+      mbar_init(id_empty(r), 1 + 4 + 4);  // MMA thread + 4 epilogue warps + 4 producer warps
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.map_a0);
-    if (MODE == kGateUp) tma_prefetch_desc(&p.map_a1);
-    if (p.has_shared) tma_prefetch_desc(&p.map_s0);
+  if (warp == 0 && lane == 0) {  // only the maps of the phases this launch runs are filled in
+    if (p.phases & 1) {
+      tma_prefetch_desc(&p.map_wg);
+      tma_prefetch_desc(&p.map_wu);
+    }
+    if (p.phases & 2) tma_prefetch_desc(&p.map_wd);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
@@ -195,7 +231,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
   pdl_wait();  // perm / offsets / activations come from the previous kernel
   pdl_launch_dependents();
 
-  // ---------------- tile list from the expert offsets (one warp)
+  // ---------------- tile lists of both phases from the expert offsets (one warp)
   const int nseg = p.E + (p.has_shared ? 1 : 0);
   if (warp == kMmaWarp) {
     for (int i = lane; i <= p.E; i += 32) seg_off[i] = __ldg(p.offsets + i);
@@ -210,146 +246,197 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
     if (!good && blockIdx.x == 0 && lane == 0 && p.err != nullptr) atomicOr(p.err, MOE_DEVERR_OFFSETS);
     const int per = (nseg + 31) / 32;
     const int s0 = lane * per;
-    int local = 0;
-    for (int s = s0; s < min(nseg, s0 + per); ++s) {
-      const bool sh = (s == p.E);
-      const int cnt = sh ? p.T : seg_off[s + 1] - seg_off[s];
-      local += good ? chunk_count<BN>(cnt) * seg_nrb<MODE>(p, sh) : 0;
-    }
-    int incl = local;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+    for (int ph = 0; ph < 2; ++ph) {
+      int *ts = ph == 0 ? start1 : start2;
+      const bool on = good && (p.phases >> ph) & 1;
+      int local = 0;
+      for (int s = s0; s < min(nseg, s0 + per); ++s)
+        local += on ? chunk_count<BN>(seg_count(p, seg_off, s)) * seg_nrb(p, ph, s == p.E) : 0;
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      int run = incl - local;
+      for (int s = s0; s < min(nseg, s0 + per); ++s) {
+        ts[s] = run;
+        run += on ? chunk_count<BN>(seg_count(p, seg_off, s)) * seg_nrb(p, ph, s == p.E) : 0;
+      }
+      if (lane == 31) ts[nseg] = incl;
     }
-    int run = incl - local;
-    for (int s = s0; s < min(nseg, s0 + per); ++s) {
-      tile_start[s] = run;
-      const bool sh = (s == p.E);
-      const int cnt = sh ? p.T : seg_off[s + 1] - seg_off[s];
-      run += good ? chunk_count<BN>(cnt) * seg_nrb<MODE>(p, sh) : 0;
-    }
-    if (lane == 31) tile_start[nseg] = incl;
   }
   __syncthreads();
-  const int total = tile_start[nseg];
+  const int total = start1[nseg] + start2[nseg];
   unsigned *err = p.err;
+  unsigned *claim = p.sync + kSyncClaim;
+  unsigned *done1 = p.sync + kSyncDone;  // gate/up tiles finished, per segment
   bool ok = true;
 
   if (warp < 4) {
     // ================= producers
-    const bool tma_thread = threadIdx.x == 0;
+    const int tid = threadIdx.x;  // 0..127
+    const int c8 = tid & 7, rbase = tid >> 3;
     const uint64_t pol_w = policy_evict_first();
     int st = 0;
     uint32_t ph = 0;
     uint32_t issued = 0, issued_par = 0;  // per stage: TMA issued, and its phase parity (thread 0)
-    if (MODE == kGateUp || warp == 0) {
-      const int tid = threadIdx.x;          // 0..127
-      const int c8 = tid & 7, rbase = tid >> 3;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<MODE, BN>(p, t, tile_start, seg_off, nseg);
-        // token rows of this thread (gate/up): rows rbase + 16 j of the chunk
-        const __nv_bfloat16 *src[BN / 16];
-        if (MODE == kGateUp) {
-          bool bad = false;
+    for (int i = 0; ok; ++i) {
+      // ---- claim the next tile (thread 0) and share its id through the ring
+      const int r = i % kRing;
+      const uint32_t rph = (uint32_t)(i / kRing) & 1u;
+      if (tid == 0) {
+        ok = mbar_wait(id_empty(r), rph ^ 1u, err, abort_flag);
+        if (ok) {
+          const int t = (int)atomicAdd(claim, 1u);
+          ring[r] = t < total ? t : -1;
+          mbar_arrive(id_full(r));
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      named_bar_sync(1, kProducers);
+      if (!ok || *abort_flag) {
+        ok = false;
+        break;
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(id_full(r), rph, err, abort_flag));
+      if (!ok) break;
+      const int t = ring[r];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(id_empty(r));
+      if (t < 0) break;
+      const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+
+      // ---- a down tile needs every gate/up tile of its segment
+      if (tl.phase == 1 && (p.phases & 1) && tid == 0) {
+        const unsigned need = (unsigned)(chunk_count<BN>(seg_count(p, seg_off, tl.seg)) * seg_nrb(p, 0, tl.shared));
+        if (ld_acquire_gpu(done1 + tl.seg) < need) {
+          const unsigned long long t0 = globaltimer();
+          while (ld_acquire_gpu(done1 + tl.seg) < need) {
+            if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
+              if (!*abort_flag && err != nullptr) atomicOr(err, MOE_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              break;
+            }
+            __nanosleep(64);
+          }
+        }
+        fence_proxy_async_global();  // the activations were written by other CTAs' generic stores
+      }
+
+      // ---- token rows of this thread for a gate/up tile: rows rbase + 16 j
+      const __nv_bfloat16 *src[BN / 16];
+      if (tl.phase == 0) {
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < BN / 16; ++j) {
+          const int row = rbase + 16 * j;
+          const int rr = row < tl.ntok ? row : 0;
+          int tok = 0;
+          if (row < tl.N) {
+            if (tl.shared) {
+              tok = tl.row0 + rr;
+            } else {
+              const int slot = __ldg(p.perm + tl.row0 + rr);
+              tok = slot / p.top_k;
+              if (slot < 0 || tok >= p.T) {
+                bad = true;
+                tok = 0;
+              }
+            }
+          }
+          src[j] = p.hidden + (size_t)tok * p.H + c8 * 8;
+        }
+        if (bad && err != nullptr) atomicOr(err, MOE_DEVERR_INDEX);
+      }
+      const int i0 = tl.rb * (tl.phase == 0 ? 128 : 256);
+      for (int kb = 0; kb < tl.nk; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(st), ph ^ 1u, err, abort_flag));
+        if (!ok || *abort_flag) {
+          ok = false;
+          break;
+        }
+        const int k0 = kb * 64;
+        if (tid == 0) {
+          const uint32_t tx = tl.phase == 0 ? (uint32_t)kABytes : (uint32_t)(kABytes + tl.N * 128);
+          mbar_arrive_expect_tx(full_bar(st), tx);
+          issued |= 1u << st;
+          issued_par = (issued_par & ~(1u << st)) | (ph << st);
+          const uint32_t a0 = a_smem(st), a1 = a0 + 16384;
+          if (tl.phase == 0) {
+            if (tl.shared) {
+              tma_load_2d_hint(a0, &p.map_sg, full_bar(st), k0, i0, pol_w);
+              tma_load_2d_hint(a1, &p.map_su, full_bar(st), k0, i0, pol_w);
+            } else {
+              tma_load_3d_hint(a0, &p.map_wg, full_bar(st), k0, i0, tl.seg, pol_w);
+              tma_load_3d_hint(a1, &p.map_wu, full_bar(st), k0, i0, tl.seg, pol_w);
+            }
+          } else {
+            if (tl.shared) {
+              tma_load_2d_hint(a0, &p.map_sd, full_bar(st), k0, i0, pol_w);
+              tma_load_2d_hint(a1, &p.map_sd, full_bar(st), k0, i0 + 128, pol_w);
+            } else {
+              tma_load_3d_hint(a0, &p.map_wd, full_bar(st), k0, i0, tl.seg, pol_w);
+              tma_load_3d_hint(a1, &p.map_wd, full_bar(st), k0, i0 + 128, tl.seg, pol_w);
+            }
+            // activation rows row0 .. row0 + N (contiguous, N a multiple of 16 and
+            // <= 256): boxes of 128 rows while they fit, then one each of 64/32/16
+            const CUtensorMap *mb = tl.shared ? p.map_acts : p.map_act;
+            int off = 0;
+            while (tl.N - off >= 128) {
+              tma_load_2d(b_smem(st) + (uint32_t)off * 128, &mb[3], full_bar(st), k0, tl.row0 + off);
+              off += 128;
+            }
+#pragma unroll
+            for (int bi = 2; bi >= 0; --bi) {
+              const int h = 16 << bi;
+              if (tl.N - off >= h) {
+                tma_load_2d(b_smem(st) + (uint32_t)off * 128, &mb[bi], full_bar(st), k0, tl.row0 + off);
+                off += h;
+              }
+            }
+          }
+        }
+        if (tl.phase == 0) {
+          const uint32_t bs = b_smem(st);
 #pragma unroll
           for (int j = 0; j < BN / 16; ++j) {
-            const int r = rbase + 16 * j;
-            const int rr = r < tl.ntok ? r : 0;
-            int tok = 0;
-            if (r < tl.N) {
-              if (tl.shared) {
-                tok = tl.row0 + rr;
-              } else {
-                const int slot = __ldg(p.perm + tl.row0 + rr);
-                tok = slot / p.top_k;
-                if (slot < 0 || tok >= p.T) {
-                  bad = true;
-                  tok = 0;
-                }
-              }
-            }
-            src[j] = p.hidden + (size_t)tok * p.H + c8 * 8;
+            const int row = rbase + 16 * j;
+            if (row < tl.N) cp_async_16(bs + row * 128 + ((c8 ^ (row & 7)) << 4), src[j] + k0);
           }
-          if (bad && err != nullptr) atomicOr(err, MOE_DEVERR_INDEX);
+          cp_async_arrive_noinc(full_bar(st));
+        } else {
+          mbar_arrive(full_bar(st));
         }
-        const int i0 = tl.rb * (MODE == kGateUp ? 128 : 256);
-        for (int kb = 0; kb < tl.nk; ++kb) {
-          ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(st), ph ^ 1u, err, abort_flag));
-          if (!ok) break;
-          const int k0 = kb * 64;
-          if (tma_thread) {
-            const uint32_t tx = MODE == kGateUp ? (uint32_t)kABytes : (uint32_t)(kABytes + tl.N * 128);
-            mbar_arrive_expect_tx(full_bar(st), tx);
-            issued |= 1u << st;
-            issued_par = (issued_par & ~(1u << st)) | (ph << st);
-            const uint32_t a0 = a_smem(st), a1 = a0 + 16384;
-            if (MODE == kGateUp) {
-              if (tl.shared) {
-                tma_load_2d_hint(a0, &p.map_s0, full_bar(st), k0, i0, pol_w);
-                tma_load_2d_hint(a1, &p.map_s1, full_bar(st), k0, i0, pol_w);
-              } else {
-                tma_load_3d_hint(a0, &p.map_a0, full_bar(st), k0, i0, tl.seg, pol_w);
-                tma_load_3d_hint(a1, &p.map_a1, full_bar(st), k0, i0, tl.seg, pol_w);
-              }
-            } else {
-              if (tl.shared) {
-                tma_load_2d_hint(a0, &p.map_s0, full_bar(st), k0, i0, pol_w);
-                tma_load_2d_hint(a1, &p.map_s0, full_bar(st), k0, i0 + 128, pol_w);
-              } else {
-                tma_load_3d_hint(a0, &p.map_a0, full_bar(st), k0, i0, tl.seg, pol_w);
-                tma_load_3d_hint(a1, &p.map_a0, full_bar(st), k0, i0 + 128, tl.seg, pol_w);
-              }
-              // activation rows row0 .. row0 + N (contiguous, N a multiple of 16 and
-              // <= 256): boxes of 128 rows while they fit, then one each of 64/32/16
-              const CUtensorMap *mb = tl.shared ? p.map_bs : p.map_b;
-              int off = 0;
-              while (tl.N - off >= 128) {
-                tma_load_2d(b_smem(st) + (uint32_t)off * 128, &mb[3], full_bar(st), k0, tl.row0 + off);
-                off += 128;
-              }
-#pragma unroll
-              for (int bi = 2; bi >= 0; --bi) {
-                const int h = 16 << bi;
-                if (tl.N - off >= h) {
-                  tma_load_2d(b_smem(st) + (uint32_t)off * 128, &mb[bi], full_bar(st), k0, tl.row0 + off);
-                  off += h;
-                }
-              }
-            }
-          }
-          if (MODE == kGateUp) {
-            const uint32_t bs = b_smem(st);
-#pragma unroll
-            for (int j = 0; j < BN / 16; ++j) {
-              const int r = rbase + 16 * j;
-              if (r < tl.N) cp_async_16(bs + r * 128 + ((c8 ^ (r & 7)) << 4), src[j] + k0);
-            }
-            cp_async_arrive_noinc(full_bar(st));
-          }
-          if (++st == STAGES) {
-            st = 0;
-            ph ^= 1u;
-          }
+        if (++st == STAGES) {
+          st = 0;
+          ph ^= 1u;
         }
       }
-      if (!ok) {
-        if (MODE == kGateUp) cp_async_wait_all();
-        if (tma_thread)
-          for (int s = 0; s < STAGES; ++s)
-            if ((issued >> s) & 1u) mbar_wait_drain(full_bar(s), (issued_par >> s) & 1u);
-      }
+    }
+    if (!ok) {
+      cp_async_wait_all();
+      if (tid == 0)
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1u) mbar_wait_drain(full_bar(s), (issued_par >> s) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // ================= MMA issuer
     if (lane == 0) {
-      int st = 0, it = 0;
+      int st = 0;
       uint32_t ph = 0;
       bool any = false;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-        const Tile tl = decode_tile<MODE, BN>(p, t, tile_start, seg_off, nseg);
-        const int acc = it % L::kAccBufs;
-        const uint32_t aph = (uint32_t)(it / L::kAccBufs) & 1u;
+      for (int i = 0; ok; ++i) {
+        const int r = i % kRing;
+        ok = mbar_wait(id_full(r), (uint32_t)(i / kRing) & 1u, err, abort_flag);
+        if (!ok) break;
+        const int t = ring[r];
+        mbar_arrive(id_empty(r));
+        if (t < 0) break;
+        const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+        const int acc = i % L::kAccBufs;
+        const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
         ok = mbar_wait(tempty_bar(acc), aph ^ 1u, err, abort_flag);
         if (!ok) break;
         tc_fence_after();
@@ -359,7 +446,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
         for (int kb = 0; kb < tl.nk; ++kb) {
           ok = mbar_wait(full_bar(st), ph, err, abort_flag);
           if (!ok) break;
-          if (MODE == kGateUp) fence_proxy_async_smem();  // token rows were written by cp.async
+          if (tl.phase == 0) fence_proxy_async_smem();  // token rows were written by cp.async
           tc_fence_after();
           const uint64_t a0 = sdesc_sw128(a_smem(st));
           const uint64_t a1 = sdesc_sw128(a_smem(st) + 16384);
@@ -389,33 +476,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
     // ================= epilogue (warps 5..8 -> TMEM lane quarters 1,2,3,0)
     const int q = warp & 3;
     const int r = 32 * q + lane;  // weight row within the 128-row half
-    int it = 0;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-      const Tile tl = decode_tile<MODE, BN>(p, t, tile_start, seg_off, nseg);
-      const int acc = it % L::kAccBufs;
-      const uint32_t aph = (uint32_t)(it / L::kAccBufs) & 1u;
+    for (int i = 0; ok; ++i) {
+      const int rs = i % kRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(id_full(rs), (uint32_t)(i / kRing) & 1u, err, abort_flag));
+      if (!ok) break;
+      const int t = ring[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(id_empty(rs));
+      if (t < 0) break;
+      const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+      const int acc = i % L::kAccBufs;
+      const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
       ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, err, abort_flag));
       if (!ok) break;
       tc_fence_after();
       const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * 2 * BN);
-      if (MODE == kGateUp) {
+      if (tl.phase == 0) {
         const int ld = tl.shared ? p.Is : p.I;
-        __nv_bfloat16 *out = tl.shared ? p.out_s : p.out;
-        const int i = tl.rb * 128 + r;
+        __nv_bfloat16 *out = tl.shared ? p.act_s : p.act;
+        const int ii = tl.rb * 128 + r;
         for (int c = 0; c < tl.N; c += 16) {
           float g[16], u[16];
           tmem_ld16(t0 + (uint32_t)c, g);
           tmem_ld16(t0 + (uint32_t)(BN + c), u);
           tmem_wait_ld();
-          if (i < ld) {
+          if (ii < ld) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               if (c + j < tl.ntok)
-                out[(size_t)(tl.row0 + c + j) * ld + i] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
+                out[(size_t)(tl.row0 + c + j) * ld + ii] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
           }
         }
       } else {
-        __nv_bfloat16 *out = tl.shared ? p.out_s : p.out;
+        __nv_bfloat16 *out = tl.shared ? p.y_s : p.y;
         const int ha = tl.rb * 256 + r, hb = ha + 128;
         for (int c = 0; c < tl.N; c += 16) {
           float va[16], vb[16];
@@ -435,6 +528,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (tl.phase == 0 && (p.phases & 2)) {
+        // publish: this gate/up tile's activations are written (release to the down tiles)
+        __threadfence();
+        named_bar_sync(2, 128);
+        if (warp == kMmaWarp + 1 && lane == 0) atomicAdd(done1 + tl.seg, 1u);
+      }
     }
   }
 
@@ -443,6 +542,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_gemm_kernel(const __gr
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
+  }
+  // the last CTA out zeroes the claim counter and the completion counts
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.sync + kSyncExit, 1u);
+    if (prev == gridDim.x - 1) {
+      volatile unsigned *s = p.sync;
+      s[kSyncClaim] = 0;
+      for (int i = 0; i < nseg; ++i) s[kSyncDone + i] = 0;
+      __threadfence();
+      s[kSyncExit] = 0;
+    }
   }
 }
 
@@ -455,40 +566,33 @@ int gemm_tile_n(int T) {
 }
 
 namespace {
-template <int MODE, int BN>
+template <int BN>
 cudaError_t launch_one(const GemmParams &p, int num_ctas, cudaStream_t stream, bool pdl) {
-  using L = Layout<MODE, BN>;
+  using L = Layout<BN>;
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(expert_ffn_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
   void *args[] = {(void *)&p};
-  return launch_ex((const void *)expert_gemm_kernel<MODE, BN>, dim3(num_ctas), dim3(kGemmThreads), L::kSmem, stream,
-                   pdl, 1, args);
-}
-
-template <int MODE>
-cudaError_t launch_mode(const GemmParams &p, int bn, int num_ctas, cudaStream_t stream, bool pdl) {
-  switch (bn) {
-    case 16: return launch_one<MODE, 16>(p, num_ctas, stream, pdl);
-    case 32: return launch_one<MODE, 32>(p, num_ctas, stream, pdl);
-    case 64: return launch_one<MODE, 64>(p, num_ctas, stream, pdl);
-    case 128: return launch_one<MODE, 128>(p, num_ctas, stream, pdl);
-    case 256: return launch_one<MODE, 256>(p, num_ctas, stream, pdl);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_ex((const void *)expert_ffn_kernel<BN>, dim3(num_ctas), dim3(kGemmThreads), L::kSmem, stream, pdl, 1,
+                   args);
 }
 }  // namespace
 
-cudaError_t launch_expert_gemm(const GemmParams &p, GemmMode mode, int bn, int num_ctas, cudaStream_t stream,
-                               bool pdl) {
-  return mode == kGateUp ? launch_mode<kGateUp>(p, bn, num_ctas, stream, pdl)
-                         : launch_mode<kDown>(p, bn, num_ctas, stream, pdl);
+cudaError_t launch_expert_ffn(const GemmParams &p, int bn, int num_ctas, cudaStream_t stream, bool pdl) {
+  switch (bn) {
+    case 16: return launch_one<16>(p, num_ctas, stream, pdl);
+    case 32: return launch_one<32>(p, num_ctas, stream, pdl);
+    case 64: return launch_one<64>(p, num_ctas, stream, pdl);
+    case 128: return launch_one<128>(p, num_ctas, stream, pdl);
+    case 256: return launch_one<256>(p, num_ctas, stream, pdl);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace moe

@@ -46,27 +46,31 @@ struct PermuteParams {
 };
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t stream, bool pdl);
 
-// ------------------------------------------------------- grouped expert GEMM
-enum GemmMode { kGateUp = 0, kDown = 1 };
+// ------------------------------------------------------- grouped expert FFN
 struct GemmParams {
-  CUtensorMap map_a0;     // gate/up: w_gate {H, I, E} box {64,128,1}; down: w_down {I, H, E} box {64,128,1}
-  CUtensorMap map_a1;     // gate/up: w_up (as map_a0); down: unused
-  CUtensorMap map_s0;     // gate/up: ws_gate {H, Is} box {64,128}; down: ws_down {Is, H} box {64,128}
-  CUtensorMap map_s1;     // gate/up: ws_up; down: unused
-  CUtensorMap map_b[4];   // down: A_act {I, S}, boxes {64, 16/32/64/128}; gate/up: unused
-  CUtensorMap map_bs[4];  // down: A_shared {Is, T}, boxes {64, 16/32/64/128}; gate/up: unused
-  const __nv_bfloat16 *hidden;  // gate/up: [T][H], read row by row through perm
+  CUtensorMap map_wg, map_wu;  // w_gate, w_up {H, I, E}, box {64,128,1}
+  CUtensorMap map_sg, map_su;  // ws_gate, ws_up {H, Is}, box {64,128}
+  CUtensorMap map_wd;          // w_down {I, H, E}, box {64,128,1}
+  CUtensorMap map_sd;          // ws_down {Is, H}, box {64,128}
+  CUtensorMap map_act[4];      // A_act {I, S}, boxes {64, 16/32/64/128}
+  CUtensorMap map_acts[4];     // A_shared {Is, T}, boxes {64, 16/32/64/128}
+  const __nv_bfloat16 *hidden;  // [T][H], read row by row through perm
   const int32_t *perm;
   const int32_t *offsets;
-  __nv_bfloat16 *out;    // gate/up: A_act [S][I]; down: y_sorted [S][H]
-  __nv_bfloat16 *out_s;  // gate/up: A_shared [T][Is]; down: y_shared [T][H]
-  unsigned *err;
+  __nv_bfloat16 *act, *act_s;  // gate/up outputs: A_act [S][I], A_shared [T][Is]
+  __nv_bfloat16 *y, *y_s;      // down outputs: y_sorted [S][H], y_shared [T][H]
+  unsigned *err;               // workspace error word
+  unsigned *sync;              // workspace header: tile claim counter, exit counter, per-segment done counts
   int T, H, E, I, Is, top_k, S, has_shared;
+  int phases;  // 1 gate/up only, 2 down only, 3 both (down tiles wait for their segment's gate/up tiles)
 };
+// word offsets into the workspace header (4 KiB, zero when the workspace is fresh;
+// every launch leaves them zero again)
+constexpr int kSyncClaim = 64, kSyncExit = 65, kSyncDone = 128;  // kSyncDone .. kSyncDone + 257
+constexpr int kWsHeaderBytes = 4096;
 constexpr int kGemmThreads = 288;  // warps 0-3 producers, 4 MMA, 5-8 epilogue
 int gemm_tile_n(int T);            // tokens per tile (multiple of 16, <= 256) chosen for a T
-cudaError_t launch_expert_gemm(const GemmParams &p, GemmMode mode, int bn, int num_ctas, cudaStream_t stream,
-                               bool pdl);
+cudaError_t launch_expert_ffn(const GemmParams &p, int bn, int num_ctas, cudaStream_t stream, bool pdl);
 
 // --------------------------------------------------------------- combine
 struct CombineParams {

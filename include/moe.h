@@ -104,7 +104,8 @@ moe_status moe_check_dims(const moe_dims *d);
  * layer's need, which covers the others); 0 when the dims are invalid. */
 size_t moe_workspace_bytes(const moe_dims *d);
 
-/* Zero the workspace header (error word and scheduler counters) on `stream`. */
+/* Zero the workspace header (error word and tile-scheduler counters, the first
+ * 4 KiB) on `stream`. */
 moe_status moe_ws_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Read (and, with clear != 0, reset) the device error word.  This is the one
