@@ -37,7 +37,9 @@
 // never wait.  The last CTA to leave zeroes the counters for the next call.
 //
 // Warp roles: 0-3 producers (warp 0 lane 0 claims tiles and issues TMA), 4
-// MMA issuer (one thread) and TMEM owner, 5-8 epilogue.  A STAGES-deep ring
+// MMA issuer (one thread) and TMEM owner, 5-12 epilogue: two warps per TMEM
+// lane quarter, each draining alternate 16-column groups, so that the
+// accumulator is released twice as fast.  A STAGES-deep ring
 // overlaps loads and MMAs; for BN <= 128 two TMEM accumulator pairs also
 // overlap one tile's epilogue with the next tile's MMAs (BN = 256 fills TMEM
 // with one pair).
@@ -52,6 +54,7 @@ constexpr int kABytes = 2 * 128 * 128;  // two 128-row x 64-bf16 weight boxes
 constexpr int kMaxSeg = 258;            // E <= 256 routed + 1 shared (+1 sentinel)
 constexpr int kProducers = 128;         // warps 0-3
 constexpr int kMmaWarp = 4;
+constexpr int kEpiWarps = 8;            // warps 5-12
 constexpr int kRing = 4;                // claimed tile ids in flight
 constexpr unsigned long long kDrainNs = 20000000ull;
 
@@ -165,7 +168,10 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// SiLU(g) * u with the fast reciprocal-based division: the result is rounded
+// to bf16, far coarser than the division's few-ulp error, and for g < -87 the
+// denominator overflows and the quotient goes to zero, which is SiLU's limit.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 }  // namespace
 
@@ -202,12 +208,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      mbar_init(tempty_bar(a), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     for (int r = 0; r < kRing; ++r) {
       mbar_init(id_full(r), 1);
-      mbar_init(id_empty(r), 1 + 4 + 4);  // MMA thread + 4 epilogue warps + 4 producer warps
+      mbar_init(id_empty(r), 1 + kEpiWarps + 4);  // MMA thread + epilogue warps + 4 producer warps
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -473,8 +479,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       }
     }
   } else {
-    // ================= epilogue (warps 5..8 -> TMEM lane quarters 1,2,3,0)
+    // ================= epilogue (warps 5..12 -> TMEM lane quarters 1,2,3,0, twice)
     const int q = warp & 3;
+    const int c_first = 16 * ((warp - kMmaWarp - 1) >> 2);  // 0 or 16: alternate column groups
     const int r = 32 * q + lane;  // weight row within the 128-row half
     for (int i = 0; ok; ++i) {
       const int rs = i % kRing;
@@ -495,7 +502,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         const int ld = tl.shared ? p.Is : p.I;
         __nv_bfloat16 *out = tl.shared ? p.act_s : p.act;
         const int ii = tl.rb * 128 + r;
-        for (int c = 0; c < tl.N; c += 16) {
+        for (int c = c_first; c < tl.N; c += 32) {
           float g[16], u[16];
           tmem_ld16(t0 + (uint32_t)c, g);
           tmem_ld16(t0 + (uint32_t)(BN + c), u);
@@ -510,7 +517,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       } else {
         __nv_bfloat16 *out = tl.shared ? p.y_s : p.y;
         const int ha = tl.rb * 256 + r, hb = ha + 128;
-        for (int c = 0; c < tl.N; c += 16) {
+        for (int c = c_first; c < tl.N; c += 32) {
           float va[16], vb[16];
           tmem_ld16(t0 + (uint32_t)c, va);
           tmem_ld16(t0 + (uint32_t)(BN + c), vb);
@@ -531,7 +538,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       if (tl.phase == 0 && (p.phases & 2)) {
         // publish: this gate/up tile's activations are written (release to the down tiles)
         __threadfence();
-        named_bar_sync(2, 128);
+        named_bar_sync(2, 32 * kEpiWarps);
         if (warp == kMmaWarp + 1 && lane == 0) atomicAdd(done1 + tl.seg, 1u);
       }
     }

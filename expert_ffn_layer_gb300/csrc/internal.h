@@ -68,7 +68,7 @@ struct GemmParams {
 // every launch leaves them zero again)
 constexpr int kSyncClaim = 64, kSyncExit = 65, kSyncDone = 128;  // kSyncDone .. kSyncDone + 257
 constexpr int kWsHeaderBytes = 4096;
-constexpr int kGemmThreads = 288;  // warps 0-3 producers, 4 MMA, 5-8 epilogue
+constexpr int kGemmThreads = 416;  // warps 0-3 producers, 4 MMA, 5-12 epilogue
 int gemm_tile_n(int T);            // tokens per tile (multiple of 16, <= 256) chosen for a T
 cudaError_t launch_expert_ffn(const GemmParams &p, int bn, int num_ctas, cudaStream_t stream, bool pdl);
 
