@@ -90,8 +90,8 @@ inline bool aligned256(const void *p) { return ((uintptr_t)p & 255u) == 0; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t err, topk_idx, topk_w, counts, offsets, perm, inv, y_sorted, y_shared, a_act, a_shared, w_hi, w_lo, partial,
-      total;
+  size_t err, topk_idx, topk_w, counts, offsets, perm, inv, perm_part, y_sorted, y_shared, a_act, a_shared, w_hi,
+      w_lo, partial, total;
 };
 
 // Split of H across router CTAs: a power of two <= 32 dividing H/64, with
@@ -122,6 +122,7 @@ WsLayout ws_layout(const moe_dims &d) {
   L.offsets = take((E + 1) * 4);
   L.perm = take(S * 4);
   L.inv = take(S * 4);
+  L.perm_part = take((size_t)permute_parts((int)S) * E * 4);
   L.y_sorted = take(S * (size_t)d.H * 2);
   L.y_shared = take(d.has_shared ? T * (size_t)d.H * 2 : 0);
   L.a_act = take(S * (size_t)d.I * 2);
@@ -192,14 +193,17 @@ moe_status do_route(const moe_dims &d, const moe_bf16 *hidden, const float *rout
 }
 
 moe_status do_permute(const moe_dims &d, const int32_t *topk_idx, int32_t *counts, int32_t *offsets, int32_t *perm,
-                      int32_t *inv, unsigned *err, cudaStream_t stream, bool pdl) {
+                      int32_t *inv, void *ws, cudaStream_t stream, bool pdl) {
+  const WsLayout L = ws_layout(d);
   PermuteParams p;
   p.topk_idx = topk_idx;
+  p.err = at<unsigned>(ws, L.err);
+  p.done = at<unsigned>(ws, L.err) + kSyncPermute;
+  p.part = at<int32_t>(ws, L.perm_part);
   p.counts = counts;
   p.offsets = offsets;
   p.perm = perm;
   p.inv = inv;
-  p.err = err;
   p.S = d.T * d.top_k;
   p.E = d.E;
   return cuda_status(launch_permute(p, stream, pdl));
@@ -381,8 +385,7 @@ MOE_API moe_status moe_permute(const moe_dims *d, const int32_t *topk_idx, int32
     if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, (size_t)(d->E + 1) * 4, s);
     return cuda_status(e);
   }
-  return do_permute(*d, topk_idx, counts, offsets, perm, inv_perm, at<unsigned>(ws, ws_layout(*d).err),
-                    (cudaStream_t)stream, true);
+  return do_permute(*d, topk_idx, counts, offsets, perm, inv_perm, ws, (cudaStream_t)stream, true);
 }
 
 MOE_API moe_status moe_expert_ffn(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
@@ -460,9 +463,7 @@ MOE_API moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, 
   int32_t *offs = at<int32_t>(ws, L.offsets);
   moe_bf16 *y = at<moe_bf16>(ws, L.y_sorted), *z = at<moe_bf16>(ws, L.y_shared);
   if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, w, ws, s, true)) != MOE_OK) return st;
-  if ((st = do_permute(*d, idx, at<int32_t>(ws, L.counts), offs, perm, inv, at<unsigned>(ws, L.err), s, true)) !=
-      MOE_OK)
-    return st;
+  if ((st = do_permute(*d, idx, at<int32_t>(ws, L.counts), offs, perm, inv, ws, s, true)) != MOE_OK) return st;
   if ((st = do_expert_ffn(*d, hidden, perm, offs, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y, z, ws, s,
                           true)) != MOE_OK)
     return st;

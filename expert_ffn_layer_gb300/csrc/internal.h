@@ -42,8 +42,15 @@ struct PermuteParams {
   int32_t *perm;            // [S]
   int32_t *inv;             // [S]
   unsigned *err;
+  int32_t *part;            // [ceil(S / kPartSlots)][E] workspace table of the many-CTA path
+  unsigned *done;           // workspace header word counting finished parts (left zero)
   int S, E;
 };
+// Batches above kPermuteOneCtaMax slots are permuted by ceil(S / kPartSlots)
+// CTAs (count + scatter kernels); smaller ones by one CTA.
+constexpr int kPartSlots = 1024;
+constexpr int kPermuteOneCtaMax = 8192;
+inline int permute_parts(int S) { return S > kPermuteOneCtaMax ? (S + kPartSlots - 1) / kPartSlots : 0; }
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t stream, bool pdl);
 
 // ------------------------------------------------------- grouped expert FFN
@@ -66,7 +73,7 @@ struct GemmParams {
 };
 // word offsets into the workspace header (4 KiB, zero when the workspace is fresh;
 // every launch leaves them zero again)
-constexpr int kSyncClaim = 64, kSyncExit = 65, kSyncDone = 128;  // kSyncDone .. kSyncDone + 257
+constexpr int kSyncClaim = 64, kSyncExit = 65, kSyncPermute = 66, kSyncDone = 128;  // kSyncDone .. kSyncDone + 257
 constexpr int kWsHeaderBytes = 4096;
 constexpr int kGemmThreads = 416;  // warps 0-3 producers, 4 MMA, 5-12 epilogue
 int gemm_tile_n(int T);            // tokens per tile (multiple of 16, <= 256) chosen for a T

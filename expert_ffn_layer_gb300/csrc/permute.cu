@@ -12,6 +12,14 @@
 // first output position; pass 2 walks the run again in slot order and ranks
 // equal experts inside a warp with match/popc, so the order inside every
 // segment is ascending slot order -- deterministic, no atomics on positions.
+//
+// Large batches (more than kPermuteOneCtaMax slots) run the same ranking on
+// many CTAs.  The slots are cut into parts of kPartSlots.  A count kernel
+// writes each part's per-expert count; the last part to finish turns the table
+// into each part's first output position per expert (a prefix over the parts
+// plus the expert offsets) and writes counts and offsets.  A scatter kernel
+// then ranks each part's slots exactly as the one-CTA kernel does, starting
+// from its row of the table, so both paths give the same permutation.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -146,9 +154,165 @@ __global__ void __launch_bounds__(kThreads, 1) permute_kernel(const PermuteParam
   if (bad && p.err != nullptr) atomicOr(p.err, MOE_DEVERR_INDEX);
 }
 
+namespace {
+constexpr int kPartThreads = 256;  // >= kMaxE: one thread per expert in the table pass
+constexpr int kPartWarps = kPartThreads / 32;
+constexpr int kWarpSlots = kPartSlots / kPartWarps;
+static_assert(kPartThreads >= kMaxE, "one thread per expert");
+static_assert(kWarpSlots % 32 == 0, "whole warp rounds");
+
+// Exclusive prefix over the block's threads (kPartThreads); returns it and sets
+// *total to the sum over all threads.
+__device__ __forceinline__ int block_excl_scan(int v, int *warp_sums, int *total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kPartWarps; ++w) {
+    const int x = warp_sums[w];
+    before += w < warp ? x : 0;
+    all += x;
+  }
+  *total = all;
+  return before + incl - v;
+}
+}  // namespace
+
+// Part g counts its slots per expert; the last part to finish builds the table.
+__global__ void __launch_bounds__(kPartThreads) permute_count_kernel(const PermuteParams p) {
+  __shared__ int cnt[kMaxE];
+  __shared__ int warp_sums[kPartWarps];
+  __shared__ int is_last;
+  const int g = blockIdx.x, G = gridDim.x, E = p.E;
+  for (int e = threadIdx.x; e < kMaxE; e += kPartThreads) cnt[e] = 0;
+
+  pdl_wait();  // topk_idx comes from the router
+  pdl_launch_dependents();
+  __syncthreads();
+
+  const int s0 = g * kPartSlots, s1 = min(p.S, s0 + kPartSlots);
+  bool bad = false;
+  for (int s = s0 + (int)threadIdx.x; s < s1; s += kPartThreads) {
+    int e = __ldg(p.topk_idx + s);
+    if (e < 0 || e >= E) {
+      bad = true;
+      e = min(max(e, 0), E - 1);
+    }
+    atomicAdd(&cnt[e], 1);
+  }
+  if (bad && p.err != nullptr) atomicOr(p.err, MOE_DEVERR_INDEX);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kPartThreads) p.part[(size_t)g * E + e] = cnt[e];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(p.done, 1u) == (unsigned)(G - 1) ? 1 : 0;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  // the last part: totals per expert, offsets, then each part's first position
+  const int e = threadIdx.x;
+  int tot = 0;
+  if (e < E)
+    for (int q = 0; q < G; ++q) tot += __ldcg(p.part + (size_t)q * E + e);
+  int all = 0;
+  const int first = block_excl_scan(e < E ? tot : 0, warp_sums, &all);
+  if (e < E) {
+    p.counts[e] = tot;
+    p.offsets[e] = first;
+    int run = first;
+    for (int q = 0; q < G; ++q) {
+      int *cell = p.part + (size_t)q * E + e;
+      const int c = __ldcg(cell);
+      *cell = run;
+      run += c;
+    }
+  }
+  if (threadIdx.x == 0) {
+    p.offsets[E] = all;
+    *p.done = 0;  // leave the header word zero for the next call
+  }
+}
+
+// Part g ranks its slots: per-warp counts, a prefix over the part's warps from
+// the part's row of the table, then the stable scatter (as the one-CTA kernel).
+__global__ void __launch_bounds__(kPartThreads) permute_scatter_kernel(const PermuteParams p) {
+  __shared__ int base[kPartWarps][kMaxE];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x, E = p.E;
+  for (int i = threadIdx.x; i < kPartWarps * kMaxE; i += kPartThreads) (&base[0][0])[i] = 0;
+
+  pdl_wait();  // the table and topk_idx come from the count kernel and the router
+  pdl_launch_dependents();
+  __syncthreads();
+
+  const int s0 = g * kPartSlots, s1 = min(p.S, s0 + kPartSlots);
+  const int w0 = min(s1, s0 + warp * kWarpSlots), w1 = min(s1, w0 + kWarpSlots);
+  constexpr int kRounds = kWarpSlots / 32;
+
+  int ev[kRounds];
+#pragma unroll
+  for (int u = 0; u < kRounds; ++u) {
+    const int s = w0 + 32 * u + lane;
+    ev[u] = s < w1 ? min(max(__ldg(p.topk_idx + s), 0), E - 1) : 0;
+  }
+#pragma unroll
+  for (int u = 0; u < kRounds; ++u) {
+    const bool valid = w0 + 32 * u + lane < w1;
+    const unsigned active = __ballot_sync(0xffffffffu, valid);
+    if (valid) {
+      const unsigned peers = __match_any_sync(active, ev[u]);
+      if (lane == __ffs(peers) - 1) base[warp][ev[u]] += __popc(peers);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int run = p.part[(size_t)g * E + e];
+#pragma unroll
+    for (int w = 0; w < kPartWarps; ++w) {
+      const int c = base[w][e];
+      base[w][e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kRounds; ++u) {
+    const int s = w0 + 32 * u + lane;
+    const bool valid = s < w1;
+    const unsigned active = __ballot_sync(0xffffffffu, valid);
+    if (valid) {
+      const int e = ev[u];
+      const unsigned peers = __match_any_sync(active, e);
+      const int leader = __ffs(peers) - 1;
+      int b = 0;
+      if (lane == leader) {
+        b = base[warp][e];
+        base[warp][e] = b + __popc(peers);
+      }
+      b = __shfl_sync(active, b, leader);
+      const int pos = b + __popc(peers & ((1u << lane) - 1u));
+      p.perm[pos] = s;
+      p.inv[s] = pos;
+    }
+  }
+}
+
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t stream, bool pdl) {
   void *args[] = {(void *)&p};
-  return launch_ex((const void *)permute_kernel, dim3(1), dim3(kThreads), 0, stream, pdl, 1, args);
+  const int G = permute_parts(p.S);
+  if (G == 0) return launch_ex((const void *)permute_kernel, dim3(1), dim3(kThreads), 0, stream, pdl, 1, args);
+  cudaError_t e = launch_ex((const void *)permute_count_kernel, dim3(G), dim3(kPartThreads), 0, stream, pdl, 1, args);
+  if (e != cudaSuccess) return e;
+  return launch_ex((const void *)permute_scatter_kernel, dim3(G), dim3(kPartThreads), 0, stream, pdl, 1, args);
 }
 
 }  // namespace moe

@@ -170,6 +170,43 @@ def _dedup(row, E):
     return np.array(out, dtype=np.int32)
 
 
+@pytest.mark.parametrize("T", [1024, 1025, 2047])
+def test_permute_one_cta_many_cta_boundary(T):
+    """S = T*8 around the switch from one CTA (S <= 8192) to 1024-slot parts, with a
+    ragged last part: both paths give the oracle's stable permutation."""
+    w = W.WORKLOADS["prefill"].with_(T=T)
+    _check_permute(w, W.synthetic_topk(w))
+
+
+def test_permute_many_cta_repeated_on_one_workspace():
+    """The part counter in the workspace header is left zero: a second call on the
+    same workspace (other indices) is exact too."""
+    w = W.WORKLOADS["prefill"].with_(T=3000)
+    d = dims_of(w)
+    dl = type("P", (), {})()
+    dl.d, dl.ws = d, moe.alloc_workspace(d)
+    for shift in (0, 17):
+        topk = np.stack([_dedup(r, w.E) for r in (W.synthetic_topk(w) + shift) % w.E])
+        counts, offsets, perm, inv = DeviceLayer.permute(dl, i32_dev(topk))
+        rp, ri = oracle.permutation(topk, w.E)
+        assert np.array_equal(perm.cpu().numpy(), rp) and np.array_equal(inv.cpu().numpy(), ri)
+        assert np.array_equal(offsets.cpu().numpy(), oracle.histogram_offsets(topk, w.E)[1])
+    assert moe.moe_ws_read_error(dl.ws) == 0
+
+
+def test_permute_many_cta_flags_out_of_range_index():
+    w = W.WORKLOADS["prefill"].with_(T=2000)
+    topk = W.synthetic_topk(w)
+    topk[1500, 2] = -3
+    d = dims_of(w)
+    dl = type("P", (), {})()
+    dl.d, dl.ws = d, moe.alloc_workspace(d)
+    counts, offsets, perm, inv = DeviceLayer.permute(dl, i32_dev(topk))
+    assert moe.moe_ws_read_error(dl.ws, clear=True) & moe.DEVERR_INDEX
+    assert int(offsets[-1]) == w.S
+    assert sorted(perm.cpu().numpy().tolist()) == list(range(w.S))
+
+
 def test_permute_flags_out_of_range_index():
     w = W.WORKLOADS["tiny"]
     topk = W.synthetic_topk(w)
