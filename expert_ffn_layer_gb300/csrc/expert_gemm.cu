@@ -36,13 +36,20 @@
 // always be satisfied, whatever the residency of other CTAs.  Gate/up tiles
 // never wait.  The last CTA to leave zeroes the counters for the next call.
 //
-// Warp roles: 0-3 producers (warp 0 lane 0 claims tiles and issues TMA), 4
-// MMA issuer (one thread) and TMEM owner, 5-12 epilogue: two warps per TMEM
-// lane quarter, each draining alternate 16-column groups, so that the
-// accumulator is released twice as fast.  A STAGES-deep ring
-// overlaps loads and MMAs; for BN <= 128 two TMEM accumulator pairs also
-// overlap one tile's epilogue with the next tile's MMAs (BN = 256 fills TMEM
-// with one pair).
+// Pipelines.  Weights stream from HBM and need the longer lead; token rows
+// come from L2.  So the two operands have rings of their own: kW weight slots
+// (both 128-row boxes of one 64-wide K step, 32 KB) and kT token slots (N rows
+// of one K step), each with full/empty barriers; the MMA of K step q takes
+// weight slot q % kW and token slot q % kT.  Narrow tiles (decode) get six
+// weight slots -- as many weight bytes in flight per SM as HBM needs -- while
+// 256-token tiles keep three of each (fewer token slots starve the MMA).
+//
+// Warp roles: 0 (one thread) claims tiles and issues the weight TMA loads; 1-4
+// load token rows (cp.async) or activation rows (TMA, one thread) and wait for
+// a down tile's gate/up tiles; 5 issues the MMAs (one thread) and owns TMEM;
+// 6-13 drain the accumulators, two warps per TMEM lane quarter on alternate
+// 16-column groups.  For BN <= 128 two TMEM accumulator pairs overlap one
+// tile's epilogue with the next tile's MMAs (BN = 256 fills TMEM with one pair).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -50,26 +57,35 @@ namespace moe {
 
 namespace {
 
-constexpr int kABytes = 2 * 128 * 128;  // two 128-row x 64-bf16 weight boxes
+constexpr int kABytes = 2 * 128 * 128;  // weights of one K step: two 128-row x 64-bf16 boxes
 constexpr int kMaxSeg = 258;            // E <= 256 routed + 1 shared (+1 sentinel)
-constexpr int kProducers = 128;         // warps 0-3
-constexpr int kMmaWarp = 4;
-constexpr int kEpiWarps = 8;            // warps 5-12
+constexpr int kWWarp = 0;               // tile claims + weight loads (lane 0)
+constexpr int kTokWarp0 = 1;            // warps 1-4: token / activation loads
+constexpr int kTokThreads = 128;
+constexpr int kMmaWarp = 5;
+constexpr int kEpiWarp0 = 6;            // warps 6-13
+constexpr int kEpiWarps = 8;
 constexpr int kRing = 4;                // claimed tile ids in flight
 constexpr unsigned long long kDrainNs = 20000000ull;
+static_assert(kGemmThreads == 32 * (kEpiWarp0 + kEpiWarps), "warp roles");
 
+// Ring depths: weight slots of 32 KB and token slots of BN x 128 bytes.
 template <int BN>
-struct StagesFor {
-  static constexpr int value = BN <= 32 ? 6 : BN <= 64 ? 5 : BN <= 128 ? 4 : 3;
+struct Rings {
+  static constexpr int kW = BN >= 256 ? 3 : BN >= 128 ? 5 : 6;
+  static constexpr int kT = BN >= 256 ? 3 : BN >= 64 ? 3 : 4;
 };
 
 template <int BN>
 struct Layout {
-  static constexpr int kStages = StagesFor<BN>::value;
-  static constexpr int kStageBytes = kABytes + BN * 128;
-  static constexpr int kBarOff = kStages * kStageBytes;
-  // full, empty per stage; tfull[2], tempty[2]; drain; id_full[kRing], id_empty[kRing]
-  static constexpr int kNumBars = 2 * kStages + 5 + 2 * kRing;
+  static constexpr int kW = Rings<BN>::kW;
+  static constexpr int kT = Rings<BN>::kT;
+  static constexpr int kTokBytes = BN * 128;
+  static constexpr int kTOff = kW * kABytes;
+  static constexpr int kBarOff = kTOff + kT * kTokBytes;
+  // wfull, wempty per weight slot; tfull, tempty per token slot; acc full[2],
+  // acc empty[2]; drain; id_full[kRing], id_empty[kRing]
+  static constexpr int kNumBars = 2 * kW + 2 * kT + 5 + 2 * kRing;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;     // tmem slot, abort flag, ring of tile ids
   static constexpr int kStart1Off = kMiscOff + 64;
   static constexpr int kStart2Off = kStart1Off + 4 * kMaxSeg;
@@ -78,9 +94,13 @@ struct Layout {
   static constexpr size_t kSmem = 1024 + kBytes;
   // accumulator pairs of 2 x BN columns: two while they fit in 512 columns, else one
   static constexpr int kAccBufs = 4 * BN <= 512 ? 2 : 1;
-  static constexpr uint32_t kTmemCols = kAccBufs * 2 * BN;
+  static constexpr uint32_t kTmemUsed = kAccBufs * 2 * BN;
+  // TMEM is allocated in powers of two columns
+  static constexpr uint32_t kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+                                        : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kSmem <= 232448, "shared memory budget");
-  static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM budget");
+  static_assert(kTmemUsed <= 512, "TMEM budget");
+  static_assert(kW <= 16 && kT <= 16, "issue masks");
 };
 
 struct Tile {
@@ -178,7 +198,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __grid_constant__ GemmParams p) {
   using L = Layout<BN>;
-  constexpr int STAGES = L::kStages;
+  constexpr int KW = L::kW, KT = L::kT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = (uint64_t *)(smem + L::kBarOff);
@@ -190,35 +210,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   int *seg_off = (int *)(smem + L::kOffOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
-  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
-  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
-  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
-  const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
-  auto id_full = [&](int r) { return smem_u32(&bars[2 * STAGES + 5 + r]); };
-  auto id_empty = [&](int r) { return smem_u32(&bars[2 * STAGES + 5 + kRing + r]); };
-  auto a_smem = [&](int s) { return smem_u32(smem + s * L::kStageBytes); };
-  auto b_smem = [&](int s) { return smem_u32(smem + s * L::kStageBytes + kABytes); };
+  auto wfull_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto wempty_bar = [&](int s) { return smem_u32(&bars[KW + s]); };
+  auto tfull_bar = [&](int s) { return smem_u32(&bars[2 * KW + s]); };
+  auto tempty_bar = [&](int s) { return smem_u32(&bars[2 * KW + KT + s]); };
+  auto afull_bar = [&](int a) { return smem_u32(&bars[2 * KW + 2 * KT + a]); };
+  auto aempty_bar = [&](int a) { return smem_u32(&bars[2 * KW + 2 * KT + 2 + a]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * KW + 2 * KT + 4]);
+  auto id_full = [&](int r) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + r]); };
+  auto id_empty = [&](int r) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + kRing + r]); };
+  auto w_smem = [&](int s) { return smem_u32(smem + s * kABytes); };
+  auto t_smem = [&](int s) { return smem_u32(smem + L::kTOff + s * L::kTokBytes); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      // 128 producer arrivals (cp.async completions or plain) + the TMA expect_tx arrival
-      mbar_init(full_bar(s), kProducers + 1);
-      mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < KW; ++s) {
+      mbar_init(wfull_bar(s), 1);   // the weight loader's expect_tx arrival
+      mbar_init(wempty_bar(s), 1);  // MMA commit
+    }
+    for (int s = 0; s < KT; ++s) {
+      mbar_init(tfull_bar(s), kTokThreads);  // one arrival per loader thread (cp.async, or the TMA expect_tx)
+      mbar_init(tempty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiWarps);
+      mbar_init(afull_bar(a), 1);
+      mbar_init(aempty_bar(a), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     for (int r = 0; r < kRing; ++r) {
       mbar_init(id_full(r), 1);
-      mbar_init(id_empty(r), 1 + kEpiWarps + 4);  // MMA thread + epilogue warps + 4 producer warps
+      mbar_init(id_empty(r), 1 + 4 + kEpiWarps);  // MMA thread + 4 token-loader warps + epilogue warps
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {  // only the maps of the phases this launch runs are filled in
+  if (warp == kWWarp && lane == 0) {  // only the maps of the phases this launch runs are filled in
     if (p.phases & 1) {
       tma_prefetch_desc(&p.map_wg);
       tma_prefetch_desc(&p.map_wu);
@@ -280,33 +305,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   unsigned *done1 = p.sync + kSyncDone;  // gate/up tiles finished, per segment
   bool ok = true;
 
-  if (warp < 4) {
-    // ================= producers
-    const int tid = threadIdx.x;  // 0..127
-    const int c8 = tid & 7, rbase = tid >> 3;
-    const uint64_t pol_w = policy_evict_first();
-    int st = 0;
-    uint32_t ph = 0;
-    uint32_t issued = 0, issued_par = 0;  // per stage: TMA issued, and its phase parity (thread 0)
-    for (int i = 0; ok; ++i) {
-      // ---- claim the next tile (thread 0) and share its id through the ring
-      const int r = i % kRing;
-      const uint32_t rph = (uint32_t)(i / kRing) & 1u;
-      if (tid == 0) {
-        ok = mbar_wait(id_empty(r), rph ^ 1u, err, abort_flag);
-        if (ok) {
-          const int t = (int)atomicAdd(claim, 1u);
-          ring[r] = t < total ? t : -1;
-          mbar_arrive(id_full(r));
+  if (warp == kWWarp) {
+    // ================= tile claims and weight loads (one thread)
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      int ws = 0;
+      uint32_t wph = 0;
+      uint32_t issued = 0, issued_par = 0;  // per weight slot: a load issued, and its phase parity
+      for (int i = 0; ok; ++i) {
+        const int r = i % kRing;
+        ok = mbar_wait(id_empty(r), ((uint32_t)(i / kRing) & 1u) ^ 1u, err, abort_flag);
+        if (!ok) break;
+        const int t0 = (int)atomicAdd(claim, 1u);
+        const int t = t0 < total ? t0 : -1;
+        ring[r] = t;
+        mbar_arrive(id_full(r));
+        if (t < 0) break;
+        const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+        const int i0 = tl.rb * (tl.phase == 0 ? 128 : 256);
+        for (int kb = 0; kb < tl.nk; ++kb) {
+          ok = mbar_wait(wempty_bar(ws), wph ^ 1u, err, abort_flag);
+          if (!ok) break;
+          const int k0 = kb * 64;
+          mbar_arrive_expect_tx(wfull_bar(ws), (uint32_t)kABytes);
+          issued |= 1u << ws;
+          issued_par = (issued_par & ~(1u << ws)) | (wph << ws);
+          const uint32_t a0 = w_smem(ws), a1 = a0 + 16384;
+          if (tl.phase == 0) {
+            if (tl.shared) {
+              tma_load_2d_hint(a0, &p.map_sg, wfull_bar(ws), k0, i0, pol_w);
+              tma_load_2d_hint(a1, &p.map_su, wfull_bar(ws), k0, i0, pol_w);
+            } else {
+              tma_load_3d_hint(a0, &p.map_wg, wfull_bar(ws), k0, i0, tl.seg, pol_w);
+              tma_load_3d_hint(a1, &p.map_wu, wfull_bar(ws), k0, i0, tl.seg, pol_w);
+            }
+          } else {
+            if (tl.shared) {
+              tma_load_2d_hint(a0, &p.map_sd, wfull_bar(ws), k0, i0, pol_w);
+              tma_load_2d_hint(a1, &p.map_sd, wfull_bar(ws), k0, i0 + 128, pol_w);
+            } else {
+              tma_load_3d_hint(a0, &p.map_wd, wfull_bar(ws), k0, i0, tl.seg, pol_w);
+              tma_load_3d_hint(a1, &p.map_wd, wfull_bar(ws), k0, i0 + 128, tl.seg, pol_w);
+            }
+          }
+          if (++ws == KW) {
+            ws = 0;
+            wph ^= 1u;
+          }
         }
       }
-      ok = __all_sync(0xffffffffu, ok);
-      named_bar_sync(1, kProducers);
-      if (!ok || *abort_flag) {
-        ok = false;
-        break;
-      }
-      ok = __all_sync(0xffffffffu, mbar_wait(id_full(r), rph, err, abort_flag));
+      if (!ok)
+        for (int s = 0; s < KW; ++s)
+          if ((issued >> s) & 1u) mbar_wait_drain(wfull_bar(s), (issued_par >> s) & 1u);
+    }
+  } else if (warp < kTokWarp0 + 4) {
+    // ================= token rows (gate/up) or activation rows (down)
+    const int tid = threadIdx.x - 32 * kTokWarp0;  // 0..127
+    const int c8 = tid & 7, rbase = tid >> 3;
+    int ts = 0;
+    uint32_t tph = 0;
+    uint32_t issued = 0, issued_par = 0;  // per token slot: an activation TMA issued (thread 0)
+    for (int i = 0; ok; ++i) {
+      const int r = i % kRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(id_full(r), (uint32_t)(i / kRing) & 1u, err, abort_flag));
       if (!ok) break;
       const int t = ring[r];
       __syncwarp();
@@ -356,82 +417,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         }
         if (bad && err != nullptr) atomicOr(err, MOE_DEVERR_INDEX);
       }
-      const int i0 = tl.rb * (tl.phase == 0 ? 128 : 256);
       for (int kb = 0; kb < tl.nk; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(empty_bar(st), ph ^ 1u, err, abort_flag));
+        ok = __all_sync(0xffffffffu, mbar_wait(tempty_bar(ts), tph ^ 1u, err, abort_flag));
         if (!ok || *abort_flag) {
           ok = false;
           break;
         }
         const int k0 = kb * 64;
-        if (tid == 0) {
-          const uint32_t tx = tl.phase == 0 ? (uint32_t)kABytes : (uint32_t)(kABytes + tl.N * 128);
-          mbar_arrive_expect_tx(full_bar(st), tx);
-          issued |= 1u << st;
-          issued_par = (issued_par & ~(1u << st)) | (ph << st);
-          const uint32_t a0 = a_smem(st), a1 = a0 + 16384;
-          if (tl.phase == 0) {
-            if (tl.shared) {
-              tma_load_2d_hint(a0, &p.map_sg, full_bar(st), k0, i0, pol_w);
-              tma_load_2d_hint(a1, &p.map_su, full_bar(st), k0, i0, pol_w);
-            } else {
-              tma_load_3d_hint(a0, &p.map_wg, full_bar(st), k0, i0, tl.seg, pol_w);
-              tma_load_3d_hint(a1, &p.map_wu, full_bar(st), k0, i0, tl.seg, pol_w);
-            }
-          } else {
-            if (tl.shared) {
-              tma_load_2d_hint(a0, &p.map_sd, full_bar(st), k0, i0, pol_w);
-              tma_load_2d_hint(a1, &p.map_sd, full_bar(st), k0, i0 + 128, pol_w);
-            } else {
-              tma_load_3d_hint(a0, &p.map_wd, full_bar(st), k0, i0, tl.seg, pol_w);
-              tma_load_3d_hint(a1, &p.map_wd, full_bar(st), k0, i0 + 128, tl.seg, pol_w);
-            }
-            // activation rows row0 .. row0 + N (contiguous, N a multiple of 16 and
-            // <= 256): boxes of 128 rows while they fit, then one each of 64/32/16
-            const CUtensorMap *mb = tl.shared ? p.map_acts : p.map_act;
-            int off = 0;
-            while (tl.N - off >= 128) {
-              tma_load_2d(b_smem(st) + (uint32_t)off * 128, &mb[3], full_bar(st), k0, tl.row0 + off);
-              off += 128;
-            }
-#pragma unroll
-            for (int bi = 2; bi >= 0; --bi) {
-              const int h = 16 << bi;
-              if (tl.N - off >= h) {
-                tma_load_2d(b_smem(st) + (uint32_t)off * 128, &mb[bi], full_bar(st), k0, tl.row0 + off);
-                off += h;
-              }
-            }
-          }
-        }
+        const uint32_t bs = t_smem(ts);
         if (tl.phase == 0) {
-          const uint32_t bs = b_smem(st);
 #pragma unroll
           for (int j = 0; j < BN / 16; ++j) {
             const int row = rbase + 16 * j;
             if (row < tl.N) cp_async_16(bs + row * 128 + ((c8 ^ (row & 7)) << 4), src[j] + k0);
           }
-          cp_async_arrive_noinc(full_bar(st));
+          cp_async_arrive_noinc(tfull_bar(ts));
+        } else if (tid == 0) {
+          // activation rows row0 .. row0 + N (contiguous, N a multiple of 16 and
+          // <= 256): boxes of 128 rows while they fit, then one each of 64/32/16
+          mbar_arrive_expect_tx(tfull_bar(ts), (uint32_t)(tl.N * 128));
+          issued |= 1u << ts;
+          issued_par = (issued_par & ~(1u << ts)) | (tph << ts);
+          const CUtensorMap *mb = tl.shared ? p.map_acts : p.map_act;
+          int off = 0;
+          while (tl.N - off >= 128) {
+            tma_load_2d(bs + (uint32_t)off * 128, &mb[3], tfull_bar(ts), k0, tl.row0 + off);
+            off += 128;
+          }
+#pragma unroll
+          for (int bi = 2; bi >= 0; --bi) {
+            const int h = 16 << bi;
+            if (tl.N - off >= h) {
+              tma_load_2d(bs + (uint32_t)off * 128, &mb[bi], tfull_bar(ts), k0, tl.row0 + off);
+              off += h;
+            }
+          }
         } else {
-          mbar_arrive(full_bar(st));
+          mbar_arrive(tfull_bar(ts));
         }
-        if (++st == STAGES) {
-          st = 0;
-          ph ^= 1u;
+        if (++ts == KT) {
+          ts = 0;
+          tph ^= 1u;
         }
       }
     }
     if (!ok) {
       cp_async_wait_all();
       if (tid == 0)
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1u) mbar_wait_drain(full_bar(s), (issued_par >> s) & 1u);
+        for (int s = 0; s < KT; ++s)
+          if ((issued >> s) & 1u) mbar_wait_drain(tfull_bar(s), (issued_par >> s) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // ================= MMA issuer
     if (lane == 0) {
-      int st = 0;
-      uint32_t ph = 0;
+      int ws = 0, ts = 0;
+      uint32_t wph = 0, tph = 0;
       bool any = false;
       for (int i = 0; ok; ++i) {
         const int r = i % kRing;
@@ -443,20 +483,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
         const int acc = i % L::kAccBufs;
         const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
-        ok = mbar_wait(tempty_bar(acc), aph ^ 1u, err, abort_flag);
+        ok = mbar_wait(aempty_bar(acc), aph ^ 1u, err, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d0 = tmem + (uint32_t)(acc * 2 * BN);
         const uint32_t d1 = d0 + (uint32_t)BN;
         const uint32_t idesc = idesc_bf16(128, tl.N);
         for (int kb = 0; kb < tl.nk; ++kb) {
-          ok = mbar_wait(full_bar(st), ph, err, abort_flag);
+          ok = mbar_wait(wfull_bar(ws), wph, err, abort_flag) && mbar_wait(tfull_bar(ts), tph, err, abort_flag);
           if (!ok) break;
           if (tl.phase == 0) fence_proxy_async_smem();  // token rows were written by cp.async
           tc_fence_after();
-          const uint64_t a0 = sdesc_sw128(a_smem(st));
-          const uint64_t a1 = sdesc_sw128(a_smem(st) + 16384);
-          const uint64_t bd = sdesc_sw128(b_smem(st));
+          const uint64_t a0 = sdesc_sw128(w_smem(ws));
+          const uint64_t a1 = sdesc_sw128(w_smem(ws) + 16384);
+          const uint64_t bd = sdesc_sw128(t_smem(ts));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
@@ -464,14 +504,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
             umma_bf16(d1, a1 + 2 * kk, bd + 2 * kk, idesc, accum);
           }
           any = true;
-          umma_commit(empty_bar(st));
-          if (++st == STAGES) {
-            st = 0;
-            ph ^= 1u;
+          umma_commit(wempty_bar(ws));
+          umma_commit(tempty_bar(ts));
+          if (++ws == KW) {
+            ws = 0;
+            wph ^= 1u;
+          }
+          if (++ts == KT) {
+            ts = 0;
+            tph ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(tfull_bar(acc));
+        umma_commit(afull_bar(acc));
       }
       if (!ok && any) {
         umma_commit(drain_bar);
@@ -479,9 +524,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       }
     }
   } else {
-    // ================= epilogue (warps 5..12 -> TMEM lane quarters 1,2,3,0, twice)
+    // ================= epilogue (warps 6..13 -> TMEM lane quarters 2,3,0,1, twice)
     const int q = warp & 3;
-    const int c_first = 16 * ((warp - kMmaWarp - 1) >> 2);  // 0 or 16: alternate column groups
+    const int c_first = 16 * ((warp - kEpiWarp0) >> 2);  // 0 or 16: alternate column groups
     const int r = 32 * q + lane;  // weight row within the 128-row half
     for (int i = 0; ok; ++i) {
       const int rs = i % kRing;
@@ -494,7 +539,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
       const int acc = i % L::kAccBufs;
       const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
-      ok = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, err, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(afull_bar(acc), aph, err, abort_flag));
       if (!ok) break;
       tc_fence_after();
       const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * 2 * BN);
@@ -534,12 +579,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) mbar_arrive(aempty_bar(acc));
       if (tl.phase == 0 && (p.phases & 2)) {
         // publish: this gate/up tile's activations are written (release to the down tiles)
         __threadfence();
         named_bar_sync(2, 32 * kEpiWarps);
-        if (warp == kMmaWarp + 1 && lane == 0) atomicAdd(done1 + tl.seg, 1u);
+        if (warp == kEpiWarp0 && lane == 0) atomicAdd(done1 + tl.seg, 1u);
       }
     }
   }
