@@ -63,11 +63,12 @@ constexpr int kWWarp = 0;               // tile claims + weight loads (lane 0)
 constexpr int kTokWarp0 = 1;            // warps 1-4: token / activation loads
 constexpr int kTokThreads = 128;
 constexpr int kMmaWarp = 5;
-constexpr int kEpiWarp0 = 6;            // warps 6-13
+constexpr int kEpiWarp0 = 6;            // warps 6.. : the epilogue
 constexpr int kEpiWarps = 8;
+constexpr int kGemmThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kWideEpiCols = 32;        // epilogue column group of tiles of 64 tokens or more
 constexpr int kRing = 4;                // claimed tile ids in flight
 constexpr unsigned long long kDrainNs = 20000000ull;
-static_assert(kGemmThreads == 32 * (kEpiWarp0 + kEpiWarps), "warp roles");
 
 // Ring depths: weight slots of 32 KB and token slots of BN x 128 bytes.
 template <int BN>
@@ -82,7 +83,11 @@ struct Layout {
   static constexpr int kT = Rings<BN>::kT;
   static constexpr int kTokBytes = BN * 128;
   static constexpr int kTOff = kW * kABytes;
-  static constexpr int kBarOff = kTOff + kT * kTokBytes;
+  // wide tiles stage each epilogue warp's 32-row x 32-token block in shared
+  // memory and store whole 16-byte pieces of token rows (2 KB per warp)
+  static constexpr bool kStageEpi = BN >= 256;
+  static constexpr int kEpiOff = kTOff + kT * kTokBytes;
+  static constexpr int kBarOff = kEpiOff + (kStageEpi ? kEpiWarps * kWideEpiCols * 64 : 0);  // tokens x 32 rows each
   // wfull, wempty per weight slot; tfull, tempty per token slot; acc full[2],
   // acc empty[2]; drain; id_full[kRing], id_empty[kRing]
   static constexpr int kNumBars = 2 * kW + 2 * kT + 5 + 2 * kRing;
@@ -526,7 +531,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   } else {
     // ================= epilogue (warps 6..13 -> TMEM lane quarters 2,3,0,1, twice)
     const int q = warp & 3;
-    const int c_first = 16 * ((warp - kEpiWarp0) >> 2);  // 0 or 16: alternate column groups
+    // column groups of kEpiCols (32 for wide tiles: one TMEM wait per 32 columns);
+    // the two warps of a lane quarter take alternate groups
+    constexpr int kEpiCols = BN >= 64 ? kWideEpiCols : 16;
+    constexpr int kEpiStep = kEpiCols * (kEpiWarps / 4);  // the lane quarter's warps take groups in turn
+    const int c_first = kEpiCols * ((warp - kEpiWarp0) >> 2);
+    __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(smem + L::kEpiOff + (warp - kEpiWarp0) * kEpiCols * 64);
     const int r = 32 * q + lane;  // weight row within the 128-row half
     for (int i = 0; ok; ++i) {
       const int rs = i % kRing;
@@ -543,36 +553,126 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       if (!ok) break;
       tc_fence_after();
       const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * 2 * BN);
-      if (tl.phase == 0) {
+      if constexpr (L::kStageEpi) {
+        // lane j of the warp owns weight row first + j; a group of ncol tokens is
+        // written to the staging block as [token][32 rows] bf16, then each lane
+        // stores 16 bytes (8 rows of one token): 4 lanes per token row piece
+        auto flush = [&](__nv_bfloat16 *rows, size_t ld, int first, int limit, int c, int ncol) {
+          __syncwarp();
+          for (int pass = 0; pass < ncol / 8; ++pass) {
+            const int jj = pass * 8 + (lane >> 2), qq = lane & 3;
+            const uint4 v = *reinterpret_cast<const uint4 *>(stage + jj * 32 + qq * 8);
+            if (c + jj < tl.ntok && first + qq * 8 < limit)
+              *reinterpret_cast<uint4 *>(rows + (size_t)(c + jj) * ld + first + qq * 8) = v;
+          }
+          __syncwarp();
+        };
+        if (tl.phase == 0) {
+          const int ld = tl.shared ? p.Is : p.I;
+          __nv_bfloat16 *rows = (tl.shared ? p.act_s : p.act) + (size_t)tl.row0 * ld;
+          const int first = tl.rb * 128 + 32 * q;
+          for (int c = c_first; c < tl.N; c += kEpiStep) {
+            float g[32], u[32];
+            const int ncol = min(kEpiCols, tl.N - c);
+            if (ncol == 32) {
+              tmem_ld32(t0 + (uint32_t)c, g);
+              tmem_ld32(t0 + (uint32_t)(BN + c), u);
+            } else {
+              tmem_ld16_lo(t0 + (uint32_t)c, g);
+              tmem_ld16_lo(t0 + (uint32_t)(BN + c), u);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < ncol) stage[j * 32 + lane] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
+            flush(rows, (size_t)ld, first, ld, c, ncol);
+          }
+        } else {
+          __nv_bfloat16 *rows = (tl.shared ? p.y_s : p.y) + (size_t)tl.row0 * p.H;
+          const int first = tl.rb * 256 + 32 * q;
+          for (int c = c_first; c < tl.N; c += kEpiStep) {
+            float va[32], vb[32];
+            const int ncol = min(kEpiCols, tl.N - c);
+            if (ncol == 32) {
+              tmem_ld32(t0 + (uint32_t)c, va);
+              tmem_ld32(t0 + (uint32_t)(BN + c), vb);
+            } else {
+              tmem_ld16_lo(t0 + (uint32_t)c, va);
+              tmem_ld16_lo(t0 + (uint32_t)(BN + c), vb);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < ncol) stage[j * 32 + lane] = __float2bfloat16_rn(va[j]);
+            flush(rows, (size_t)p.H, first, p.H, c, ncol);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < ncol) stage[j * 32 + lane] = __float2bfloat16_rn(vb[j]);
+            flush(rows, (size_t)p.H, first + 128, p.H, c, ncol);
+          }
+        }
+      } else if (tl.phase == 0) {
         const int ld = tl.shared ? p.Is : p.I;
         __nv_bfloat16 *out = tl.shared ? p.act_s : p.act;
         const int ii = tl.rb * 128 + r;
-        for (int c = c_first; c < tl.N; c += 32) {
-          float g[16], u[16];
-          tmem_ld16(t0 + (uint32_t)c, g);
-          tmem_ld16(t0 + (uint32_t)(BN + c), u);
-          tmem_wait_ld();
-          if (ii < ld) {
+        for (int c = c_first; c < tl.N; c += kEpiStep) {
+          if (kEpiCols == 32 && c + 32 <= tl.N) {
+            float g[32], u[32];
+            tmem_ld32(t0 + (uint32_t)c, g);
+            tmem_ld32(t0 + (uint32_t)(BN + c), u);
+            tmem_wait_ld();
+            if (ii < ld) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c + j < tl.ntok)
-                out[(size_t)(tl.row0 + c + j) * ld + ii] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
+              for (int j = 0; j < 32; ++j)
+                if (c + j < tl.ntok)
+                  out[(size_t)(tl.row0 + c + j) * ld + ii] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
+            }
+          } else {
+            for (int c16 = c; c16 < min(c + kEpiCols, tl.N); c16 += 16) {
+              float g[16], u[16];
+              tmem_ld16(t0 + (uint32_t)c16, g);
+              tmem_ld16(t0 + (uint32_t)(BN + c16), u);
+              tmem_wait_ld();
+              if (ii < ld) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (c16 + j < tl.ntok)
+                    out[(size_t)(tl.row0 + c16 + j) * ld + ii] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
+              }
+            }
           }
         }
       } else {
         __nv_bfloat16 *out = tl.shared ? p.y_s : p.y;
         const int ha = tl.rb * 256 + r, hb = ha + 128;
-        for (int c = c_first; c < tl.N; c += 32) {
-          float va[16], vb[16];
-          tmem_ld16(t0 + (uint32_t)c, va);
-          tmem_ld16(t0 + (uint32_t)(BN + c), vb);
-          tmem_wait_ld();
+        for (int c = c_first; c < tl.N; c += kEpiStep) {
+          if (kEpiCols == 32 && c + 32 <= tl.N) {
+            float va[32], vb[32];
+            tmem_ld32(t0 + (uint32_t)c, va);
+            tmem_ld32(t0 + (uint32_t)(BN + c), vb);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c + j < tl.ntok) {
-              __nv_bfloat16 *row = out + (size_t)(tl.row0 + c + j) * p.H;
-              if (ha < p.H) row[ha] = __float2bfloat16_rn(va[j]);
-              if (hb < p.H) row[hb] = __float2bfloat16_rn(vb[j]);
+            for (int j = 0; j < 32; ++j) {
+              if (c + j < tl.ntok) {
+                __nv_bfloat16 *row = out + (size_t)(tl.row0 + c + j) * p.H;
+                if (ha < p.H) row[ha] = __float2bfloat16_rn(va[j]);
+                if (hb < p.H) row[hb] = __float2bfloat16_rn(vb[j]);
+              }
+            }
+          } else {
+            for (int c16 = c; c16 < min(c + kEpiCols, tl.N); c16 += 16) {
+              float va[16], vb[16];
+              tmem_ld16(t0 + (uint32_t)c16, va);
+              tmem_ld16(t0 + (uint32_t)(BN + c16), vb);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (c16 + j < tl.ntok) {
+                  __nv_bfloat16 *row = out + (size_t)(tl.row0 + c16 + j) * p.H;
+                  if (ha < p.H) row[ha] = __float2bfloat16_rn(va[j]);
+                  if (hb < p.H) row[hb] = __float2bfloat16_rn(vb[j]);
+                }
+              }
             }
           }
         }

@@ -75,7 +75,6 @@ struct GemmParams {
 // every launch leaves them zero again)
 constexpr int kSyncClaim = 64, kSyncExit = 65, kSyncPermute = 66, kSyncDone = 128;  // kSyncDone .. kSyncDone + 257
 constexpr int kWsHeaderBytes = 4096;
-constexpr int kGemmThreads = 448;  // warp 0 claims + weights, 1-4 tokens, 5 MMA, 6-13 epilogue
 int gemm_tile_n(int T);            // tokens per tile (multiple of 16, <= 256) chosen for a T
 cudaError_t launch_expert_ffn(const GemmParams &p, int bn, int num_ctas, cudaStream_t stream, bool pdl);
 

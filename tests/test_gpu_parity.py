@@ -257,6 +257,30 @@ def test_expert_ffn_skewed_segments(T):
     assert_layer_close(host_f64(y), y_ref, "skewed y_sorted")
 
 
+def test_expert_ffn_odd_row_blocks_and_chunks():
+    """Wide tiles with odd row-block counts (I = 384: three gate/up blocks; H = 768:
+    three down blocks), an expert of three uneven chunks, one of ten tokens (a
+    16-row activation tile), empty experts, and a one-block shared expert
+    (I = 128) of three chunks."""
+    w = W.Workload("pair_odd", 700, 768, 6, 2, 384, 128, "sigmoid", 2.826, 0.0, True, "normal", 0.1, 11)
+    inp = W.layer_inputs(w)
+    t = np.arange(w.T)
+    topk = np.zeros((w.T, 2), dtype=np.int32)
+    topk[:, 1] = np.where(t % 2 == 0, 4, np.where(t % 35 == 1, 2, 5))
+    counts, offsets = oracle.histogram_offsets(topk, w.E)
+    assert counts.tolist() == [700, 0, 10, 0, 350, 340]
+    perm, inv = oracle.permutation(topk, w.E)
+    y_ref = oracle.expert_outputs_sorted(inp["hidden"], perm, offsets, w.top_k, inp["w_gate"], inp["w_up"],
+                                         inp["w_down"])
+    z_ref = oracle.shared_expert(inp["hidden"], inp["ws_gate"], inp["ws_up"], inp["ws_down"])
+    dl = DeviceLayer(w, inp)
+    y, z = dl.expert_ffn(i32_dev(perm), i32_dev(offsets))
+    torch.cuda.synchronize()
+    assert_layer_close(host_f64(y), y_ref, "pair_odd y_sorted")
+    assert_layer_close(host_f64(z), z_ref, "pair_odd y_shared")
+    assert moe.moe_ws_read_error(dl.ws) == 0
+
+
 def test_expert_ffn_decode_shape():
     """Hy3 decode shape (T = 8, 192 experts, I = 1536): N = 16 tiles, deep pipelines."""
     w = W.WORKLOADS["decode"]
