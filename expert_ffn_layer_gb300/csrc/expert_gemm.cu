@@ -9,54 +9,47 @@
 // SwiGLU experts down(SiLU(gate(x)) * up(x)), stacked expert weights, the
 // shared MLP applied to every token.
 //
-// Tiles.  Weight rows are the M operand of every MMA and the tokens of one
-// expert chunk are the N operand (at most BN <= 256).  Two MMAs per K step
-// share one token tile and accumulate into two TMEM accumulators:
-//   gate/up tile: D0 = gate rows, D1 = the up rows of the same indices, so gate
+// Tiles.  Weight rows are the M = 128 operand of every MMA and the tokens of
+// one expert chunk are the N operand (N = tokens rounded up to 16, at most
+// BN <= 256).  A tile is 256 weight rows x N tokens: two MMAs per K step share
+// one token tile and accumulate into two TMEM accumulators,
+//   gate/up tile: D0 = gate rows i0..i0+127, D1 = up rows i0..i0+127, so gate
 //                 row i and up row i land in the same TMEM lane and one thread
 //                 forms SiLU(gate) * up -> bf16 activation A_act[p][i];
-//   down tile:    D0, D1 = two blocks of w_down rows -> y[p][h].
-// Narrow tiles (BN <= 128, small batches) run one CTA per tile with M = 128:
-// 128 gate + 128 up rows, or 256 down rows.  256-token tiles run on CTA pairs
-// (clusters of two) with the 2-SM MMA, M = 256: the pair's tile is 256 gate +
-// 256 up rows (512 down rows) x N tokens; each CTA holds its 128 rows of every
-// weight block and half of the token rows, and the first CTA's MMAs read the
-// other half from its partner's shared memory.  Per SM that is 48 KB of
-// operands per K step instead of 64 KB for the same tensor work -- the bytes
-// that enter each SM are what bound these tiles.
+//   down tile:    D0 = w_down rows h0..h0+127, D1 = rows h0+128..h0+255 ->
+//                 y[p][h].
+// Sharing the token tile between 256 weight rows halves the token re-reads.
 //
-// Operand loads per 64-wide K step: the 128-row weight boxes by TMA (128-byte
-// swizzle); the token rows of a gate/up tile through the route index (token =
-// perm[p] / k) by cp.async from 128 threads straight from `hidden`, written in
-// the same swizzled layout (TMA's 4-row gather tops out far below the rate
-// these tiles need); the activation rows of a down tile, which are contiguous,
-// by at most four TMA boxes.
+// Operand loads per 64-wide K step: the two 128-row weight boxes by TMA
+// (128-byte swizzle); the token rows of a gate/up tile through the route index
+// (token = perm[p] / k) by cp.async from 128 producer threads straight from
+// `hidden`, written in the same swizzled layout (TMA's 4-row gather tops out
+// far below the rate these tiles need); the activation rows of a down tile,
+// which are contiguous, by at most four TMA boxes.
 //
-// Scheduling.  The tile list is every gate/up tile (per segment: row blocks x
-// token chunks, chunks innermost so they reuse the block's weights in L2)
-// followed by every down tile.  CTAs (one per SM; pairs claim through their
-// first CTA) claim tiles in that order from an atomic counter, so a down tile
-// is claimed only after every gate/up tile has been claimed by a running CTA:
-// its wait for the gate/up tiles of its segment (a per-segment completion
-// count, bounded) can always be satisfied, whatever the residency of other
-// CTAs.  Gate/up tiles never wait.  The last CTA to leave zeroes the counters.
+// Scheduling.  The tile list is every gate/up tile (per segment: 128-row
+// blocks of I x token chunks, chunks innermost so they reuse the block's
+// weights in L2) followed by every down tile.  CTAs (one per SM) claim tiles
+// in that order from an atomic counter, so a down tile is claimed only after
+// every gate/up tile has been claimed by a running CTA: its wait for the
+// gate/up tiles of its segment (a per-segment completion count, bounded) can
+// always be satisfied, whatever the residency of other CTAs.  Gate/up tiles
+// never wait.  The last CTA to leave zeroes the counters for the next call.
 //
-// Pipelines.  The two operands have rings of their own: kW weight slots (both
-// 128-row boxes of one K step, 32 KB) and kT token slots (the CTA's token rows
+// Pipelines.  Weights stream from HBM and need the longer lead; token rows
+// come from L2.  So the two operands have rings of their own: kW weight slots
+// (both 128-row boxes of one 64-wide K step, 32 KB) and kT token slots (N rows
 // of one K step), each with full/empty barriers; the MMA of K step q takes
-// weight slot q % kW and token slot q % kT.  In a pair the first CTA's MMA
-// thread also waits for the partner's slots: the partner's otherwise idle MMA
-// thread relays their completion with an asynchronous 4-byte store into the
-// first CTA that completes a transaction on a third ring of barriers (a plain
-// remote arrive with cluster-scope release blocks the relaying thread for more
-// than a K step of MMAs), and the MMA commits release the slots of both CTAs.
+// weight slot q % kW and token slot q % kT.  Narrow tiles (decode) get six
+// weight slots -- as many weight bytes in flight per SM as HBM needs -- while
+// 256-token tiles keep three of each (fewer token slots starve the MMA).
 //
 // Warp roles: 0 (one thread) claims tiles and issues the weight TMA loads; 1-4
 // load token rows (cp.async) or activation rows (TMA, one thread) and wait for
-// a down tile's gate/up tiles; 5 issues the MMAs (one thread; in a pair's
-// second CTA it relays) and owns TMEM; 6-13 drain the accumulators, two warps
-// per TMEM lane quarter on alternate column groups.  For BN <= 128 two TMEM
-// accumulator pairs overlap one tile's epilogue with the next tile's MMAs.
+// a down tile's gate/up tiles; 5 issues the MMAs (one thread) and owns TMEM;
+// 6-13 drain the accumulators, two warps per TMEM lane quarter on alternate
+// 16-column groups.  For BN <= 128 two TMEM accumulator pairs overlap one
+// tile's epilogue with the next tile's MMAs (BN = 256 fills TMEM with one pair).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -75,32 +68,30 @@ constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kWideEpiCols = 32;        // epilogue column group of tiles of 64 tokens or more
 constexpr int kRing = 4;                // claimed tile ids in flight
-constexpr uint16_t kBoth = 3;           // cluster mask of a CTA pair
 constexpr unsigned long long kDrainNs = 20000000ull;
 
-// Ring depths: weight slots of 32 KB, token slots of the CTA's token rows.
-template <int BN, bool PAIR>
+// Ring depths: weight slots of 32 KB and token slots of BN x 128 bytes.
+template <int BN>
 struct Rings {
-  static constexpr int kW = PAIR ? 4 : BN >= 256 ? 3 : BN >= 128 ? 5 : 6;
-  static constexpr int kT = PAIR ? 4 : BN >= 256 ? 3 : BN >= 64 ? 3 : 4;
+  static constexpr int kW = BN >= 256 ? 3 : BN >= 128 ? 5 : 6;
+  static constexpr int kT = BN >= 256 ? 3 : BN >= 64 ? 3 : 4;
 };
 
-template <int BN, bool PAIR>
+template <int BN>
 struct Layout {
-  static constexpr int kW = Rings<BN, PAIR>::kW;
-  static constexpr int kT = Rings<BN, PAIR>::kT;
-  static constexpr int kTokRows = PAIR ? BN / 2 : BN;  // token rows a CTA holds per K step
-  static constexpr int kTokBytes = kTokRows * 128;
+  static constexpr int kW = Rings<BN>::kW;
+  static constexpr int kT = Rings<BN>::kT;
+  static constexpr int kTokBytes = BN * 128;
   static constexpr int kTOff = kW * kABytes;
   // wide tiles stage each epilogue warp's 32-row x 32-token block in shared
   // memory and store whole 16-byte pieces of token rows (2 KB per warp)
   static constexpr bool kStageEpi = BN >= 256;
   static constexpr int kEpiOff = kTOff + kT * kTokBytes;
-  static constexpr int kBarOff = kEpiOff + (kStageEpi ? kEpiWarps * kWideEpiCols * 64 : 0);
-  // wfull, wempty per weight slot; tfull, tempty, pfull (partner ready) per
-  // token slot; acc full[2], acc empty[2]; drain; id_full[kRing], id_empty[kRing]
-  static constexpr int kNumBars = 2 * kW + 3 * kT + 5 + 2 * kRing;
-  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem slot, abort flag, ring of tile ids, relay words
+  static constexpr int kBarOff = kEpiOff + (kStageEpi ? kEpiWarps * kWideEpiCols * 64 : 0);  // tokens x 32 rows each
+  // wfull, wempty per weight slot; tfull, tempty per token slot; acc full[2],
+  // acc empty[2]; drain; id_full[kRing], id_empty[kRing]
+  static constexpr int kNumBars = 2 * kW + 2 * kT + 5 + 2 * kRing;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;     // tmem slot, abort flag, ring of tile ids
   static constexpr int kStart1Off = kMiscOff + 64;
   static constexpr int kStart2Off = kStart1Off + 4 * kMaxSeg;
   static constexpr int kOffOff = kStart2Off + 4 * kMaxSeg;
@@ -114,8 +105,7 @@ struct Layout {
                                         : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kTmemUsed <= 512, "TMEM budget");
-  static_assert(kW <= 16 && kT <= 8, "issue masks, relay words");
-  static_assert(!PAIR || BN == 256, "CTA pairs run the 256-token tiles");
+  static_assert(kW <= 16 && kT <= 16, "issue masks");
 };
 
 struct Tile {
@@ -124,39 +114,31 @@ struct Tile {
 };
 
 // Tokens per chunk for a segment of `cnt` tokens: the fewest chunks of at most
-// BN tokens, made as even as possible and rounded up to 16 (32 for a pair,
-// whose CTAs hold half each).
-template <int BN, bool PAIR>
+// BN tokens, made as even as possible and rounded up to 16.
+template <int BN>
 __device__ __forceinline__ int chunk_base(int cnt) {
-  constexpr int q = PAIR ? 32 : 16;
   const int n0 = (cnt + BN - 1) / BN;
   const int per = (cnt + n0 - 1) / n0;
-  return (per + q - 1) & ~(q - 1);
+  return (per + 15) & ~15;
 }
-template <int BN, bool PAIR>
+template <int BN>
 __device__ __forceinline__ int chunk_count(int cnt) {
   if (cnt <= 0) return 0;
-  const int b = chunk_base<BN, PAIR>(cnt);
+  const int b = chunk_base<BN>(cnt);
   return (cnt + b - 1) / b;
 }
 
-// Weight rows of a tile: gate/up 128 (pair: 256) gate/up row pairs; down 256
-// (pair: 512) rows of w_down.
-template <bool PAIR>
-__device__ __forceinline__ int tile_rows(int phase) {
-  return (phase == 0 ? 128 : 256) * (PAIR ? 2 : 1);
-}
-template <bool PAIR>
+// Weight row blocks of a segment: 128 gate/up pairs, or 256 rows of w_down.
 __device__ __forceinline__ int seg_nrb(const GemmParams &p, int phase, bool shared) {
-  const int rows = phase == 0 ? (shared ? p.Is : p.I) : p.H;
-  return (rows + tile_rows<PAIR>(phase) - 1) / tile_rows<PAIR>(phase);
+  if (phase == 0) return ((shared ? p.Is : p.I) + 127) >> 7;
+  return (p.H + 255) >> 8;
 }
 
 __device__ __forceinline__ int seg_count(const GemmParams &p, const int *seg_off, int s) {
   return s == p.E ? p.T : seg_off[s + 1] - seg_off[s];
 }
 
-template <int BN, bool PAIR>
+template <int BN>
 __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const int *start1, const int *start2,
                                             const int *seg_off, int nseg) {
   Tile tl;
@@ -172,15 +154,15 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const in
   tl.seg = lo;
   tl.shared = (lo == p.E) ? 1 : 0;
   const int cnt = seg_count(p, seg_off, lo);
-  const int nch = chunk_count<BN, PAIR>(cnt);
+  const int nch = chunk_count<BN>(cnt);
   const int local = u - ts[lo];
   tl.rb = local / nch;
   const int ch = local - tl.rb * nch;
-  const int base = chunk_base<BN, PAIR>(cnt);
+  const int base = chunk_base<BN>(cnt);
   const int pin = ch * base;
   tl.ntok = min(base, cnt - pin);
   tl.row0 = (tl.shared ? 0 : seg_off[lo]) + pin;
-  tl.N = PAIR ? (tl.ntok + 31) & ~31 : (tl.ntok + 15) & ~15;
+  tl.N = (tl.ntok + 15) & ~15;
   tl.nk = tl.phase == 0 ? (p.H >> 6) : ((tl.shared ? p.Is : p.I) >> 6);
   return tl;
 }
@@ -218,9 +200,9 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 
 }  // namespace
 
-template <int BN, bool PAIR>
+template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __grid_constant__ GemmParams p) {
-  using L = Layout<BN, PAIR>;
+  using L = Layout<BN>;
   constexpr int KW = L::kW, KT = L::kT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -228,49 +210,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   uint32_t *tmem_slot = (uint32_t *)(smem + L::kMiscOff);
   volatile int *abort_flag = (volatile int *)(smem + L::kMiscOff + 4);
   volatile int *ring = (volatile int *)(smem + L::kMiscOff + 16);  // kRing claimed tile ids
-  uint32_t *relay_word = (uint32_t *)(smem + L::kMiscOff + 32);    // pair: one per token slot (<= 8)
   int *start1 = (int *)(smem + L::kStart1Off);
   int *start2 = (int *)(smem + L::kStart2Off);
   int *seg_off = (int *)(smem + L::kOffOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = PAIR ? (int)cluster_ctarank() : 0;  // 0: the pair's MMA-issuing CTA
   auto wfull_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto wempty_bar = [&](int s) { return smem_u32(&bars[KW + s]); };
   auto tfull_bar = [&](int s) { return smem_u32(&bars[2 * KW + s]); };
   auto tempty_bar = [&](int s) { return smem_u32(&bars[2 * KW + KT + s]); };
-  auto pfull_bar = [&](int s) { return smem_u32(&bars[2 * KW + 2 * KT + s]); };
-  auto afull_bar = [&](int a) { return smem_u32(&bars[2 * KW + 3 * KT + a]); };
-  auto aempty_bar = [&](int a) { return smem_u32(&bars[2 * KW + 3 * KT + 2 + a]); };
-  const uint32_t drain_bar = smem_u32(&bars[2 * KW + 3 * KT + 4]);
-  auto id_full = [&](int r) { return smem_u32(&bars[2 * KW + 3 * KT + 5 + r]); };
-  auto id_empty = [&](int r) { return smem_u32(&bars[2 * KW + 3 * KT + 5 + kRing + r]); };
+  auto afull_bar = [&](int a) { return smem_u32(&bars[2 * KW + 2 * KT + a]); };
+  auto aempty_bar = [&](int a) { return smem_u32(&bars[2 * KW + 2 * KT + 2 + a]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * KW + 2 * KT + 4]);
+  auto id_full = [&](int r) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + r]); };
+  auto id_empty = [&](int r) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + kRing + r]); };
   auto w_smem = [&](int s) { return smem_u32(smem + s * kABytes); };
   auto t_smem = [&](int s) { return smem_u32(smem + L::kTOff + s * L::kTokBytes); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < KW; ++s) {
       mbar_init(wfull_bar(s), 1);   // the weight loader's expect_tx arrival
-      mbar_init(wempty_bar(s), 1);  // the (pair's) MMA commit
+      mbar_init(wempty_bar(s), 1);  // MMA commit
     }
     for (int s = 0; s < KT; ++s) {
       mbar_init(tfull_bar(s), kTokThreads);  // one arrival per loader thread (cp.async, or the TMA expect_tx)
       mbar_init(tempty_bar(s), 1);
-      mbar_init(pfull_bar(s), 1);  // pair: the MMA thread's expect_tx; the partner's relay brings the bytes
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(afull_bar(a), 1);
-      // a pair's accumulators live in both CTAs: both epilogues release them
-      mbar_init(aempty_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps);
+      mbar_init(aempty_bar(a), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
-    // claimed ids are read by the MMA thread, 4 token-loader warps and the
-    // epilogue warps, and in a pair also by the second CTA's weight loader;
-    // the pair's first CTA claims for both
-    const uint32_t n_id = PAIR ? 2 * (1 + 4 + kEpiWarps) + 1 : 1 + 4 + kEpiWarps;
     for (int r = 0; r < kRing; ++r) {
       mbar_init(id_full(r), 1);
-      mbar_init(id_empty(r), n_id);
+      mbar_init(id_empty(r), 1 + 4 + kEpiWarps);  // MMA thread + 4 token-loader warps + epilogue warps
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -283,17 +256,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
     if (p.phases & 2) tma_prefetch_desc(&p.map_wd);
   }
   if (warp == kMmaWarp) {
-    if constexpr (PAIR) {
-      tmem_alloc_pair(smem_u32(tmem_slot), L::kTmemCols);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
-      tmem_relinquish();
-    }
+    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (PAIR) cluster_sync();  // the partner's barriers exist before anything reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -321,7 +288,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       const bool on = good && (p.phases >> ph) & 1;
       int local = 0;
       for (int s = s0; s < min(nseg, s0 + per); ++s)
-        local += on ? chunk_count<BN, PAIR>(seg_count(p, seg_off, s)) * seg_nrb<PAIR>(p, ph, s == p.E) : 0;
+        local += on ? chunk_count<BN>(seg_count(p, seg_off, s)) * seg_nrb(p, ph, s == p.E) : 0;
       int incl = local;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -331,7 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       int run = incl - local;
       for (int s = s0; s < min(nseg, s0 + per); ++s) {
         ts[s] = run;
-        run += on ? chunk_count<BN, PAIR>(seg_count(p, seg_off, s)) * seg_nrb<PAIR>(p, ph, s == p.E) : 0;
+        run += on ? chunk_count<BN>(seg_count(p, seg_off, s)) * seg_nrb(p, ph, s == p.E) : 0;
       }
       if (lane == 31) ts[nseg] = incl;
     }
@@ -340,26 +307,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   const int total = start1[nseg] + start2[nseg];
   unsigned *err = p.err;
   unsigned *claim = p.sync + kSyncClaim;
-  unsigned *done1 = p.sync + kSyncDone;  // gate/up tiles finished, per segment (one count per CTA of a tile)
+  unsigned *done1 = p.sync + kSyncDone;  // gate/up tiles finished, per segment
   bool ok = true;
 
-  // claimed ids: wait for one / hand its slot back (to the claiming CTA)
-  auto wait_id = [&](int r, uint32_t parity) -> bool {
-    if constexpr (PAIR) return mbar_wait_cluster(id_full(r), parity, err, abort_flag);
-    else return mbar_wait(id_full(r), parity, err, abort_flag);
-  };
-  auto release_id = [&](int r) {
-    if constexpr (PAIR) {
-      if (rank != 0) {
-        mbar_arrive_cluster(map_cluster(id_empty(r), 0));
-        return;
-      }
-    }
-    mbar_arrive(id_empty(r));
-  };
-
   if (warp == kWWarp) {
-    // ================= claims (first CTA) and weight loads (one thread)
+    // ================= tile claims and weight loads (one thread)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       int ws = 0;
@@ -367,30 +319,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       uint32_t issued = 0, issued_par = 0;  // per weight slot: a load issued, and its phase parity
       for (int i = 0; ok; ++i) {
         const int r = i % kRing;
-        const uint32_t rph = (uint32_t)(i / kRing) & 1u;
-        int t;
-        if (rank == 0) {
-          ok = mbar_wait(id_empty(r), rph ^ 1u, err, abort_flag);
-          if (!ok) break;
-          const int t0 = (int)atomicAdd(claim, 1u);
-          t = t0 < total ? t0 : -1;
-          ring[r] = t;
-          if constexpr (PAIR) {
-            st_cluster_u32(map_cluster(smem_u32(const_cast<int *>(ring + r)), 1), (uint32_t)t);
-            mbar_arrive_cluster(map_cluster(id_full(r), 1));
-          }
-          mbar_arrive(id_full(r));
-        } else {
-          ok = wait_id(r, rph);
-          if (!ok) break;
-          t = ring[r];
-          release_id(r);
-        }
+        ok = mbar_wait(id_empty(r), ((uint32_t)(i / kRing) & 1u) ^ 1u, err, abort_flag);
+        if (!ok) break;
+        const int t0 = (int)atomicAdd(claim, 1u);
+        const int t = t0 < total ? t0 : -1;
+        ring[r] = t;
+        mbar_arrive(id_full(r));
         if (t < 0) break;
-        const Tile tl = decode_tile<BN, PAIR>(p, t, start1, start2, seg_off, nseg);
-        // this CTA's 128 rows of each weight block of the tile
-        const int i0 = tl.rb * tile_rows<PAIR>(tl.phase) + rank * 128;
-        const int i1 = i0 + tile_rows<PAIR>(tl.phase) / 2;  // down: the second block
+        const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+        const int i0 = tl.rb * (tl.phase == 0 ? 128 : 256);
         for (int kb = 0; kb < tl.nk; ++kb) {
           ok = mbar_wait(wempty_bar(ws), wph ^ 1u, err, abort_flag);
           if (!ok) break;
@@ -410,10 +347,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
           } else {
             if (tl.shared) {
               tma_load_2d_hint(a0, &p.map_sd, wfull_bar(ws), k0, i0, pol_w);
-              tma_load_2d_hint(a1, &p.map_sd, wfull_bar(ws), k0, i1, pol_w);
+              tma_load_2d_hint(a1, &p.map_sd, wfull_bar(ws), k0, i0 + 128, pol_w);
             } else {
               tma_load_3d_hint(a0, &p.map_wd, wfull_bar(ws), k0, i0, tl.seg, pol_w);
-              tma_load_3d_hint(a1, &p.map_wd, wfull_bar(ws), k0, i1, tl.seg, pol_w);
+              tma_load_3d_hint(a1, &p.map_wd, wfull_bar(ws), k0, i0 + 128, tl.seg, pol_w);
             }
           }
           if (++ws == KW) {
@@ -435,21 +372,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
     uint32_t issued = 0, issued_par = 0;  // per token slot: an activation TMA issued (thread 0)
     for (int i = 0; ok; ++i) {
       const int r = i % kRing;
-      ok = __all_sync(0xffffffffu, wait_id(r, (uint32_t)(i / kRing) & 1u));
+      ok = __all_sync(0xffffffffu, mbar_wait(id_full(r), (uint32_t)(i / kRing) & 1u, err, abort_flag));
       if (!ok) break;
       const int t = ring[r];
       __syncwarp();
-      if (lane == 0) release_id(r);
+      if (lane == 0) mbar_arrive(id_empty(r));
       if (t < 0) break;
-      const Tile tl = decode_tile<BN, PAIR>(p, t, start1, start2, seg_off, nseg);
-      // this CTA's token rows of the chunk: all N, or in a pair its half
-      const int tok_n = PAIR ? tl.N >> 1 : tl.N;
-      const int tok_lo = rank * tok_n;
+      const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
 
       // ---- a down tile needs every gate/up tile of its segment
       if (tl.phase == 1 && (p.phases & 1) && tid == 0) {
-        const unsigned need = (unsigned)(chunk_count<BN, PAIR>(seg_count(p, seg_off, tl.seg)) *
-                                         seg_nrb<PAIR>(p, 0, tl.shared) * (PAIR ? 2 : 1));
+        const unsigned need = (unsigned)(chunk_count<BN>(seg_count(p, seg_off, tl.seg)) * seg_nrb(p, 0, tl.shared));
         if (ld_acquire_gpu(done1 + tl.seg) < need) {
           const unsigned long long t0 = globaltimer();
           while (ld_acquire_gpu(done1 + tl.seg) < need) {
@@ -465,16 +398,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       }
 
       // ---- token rows of this thread for a gate/up tile: rows rbase + 16 j
-      const __nv_bfloat16 *src[L::kTokRows / 16];
+      const __nv_bfloat16 *src[BN / 16];
       if (tl.phase == 0) {
         bool bad = false;
 #pragma unroll
-        for (int j = 0; j < L::kTokRows / 16; ++j) {
+        for (int j = 0; j < BN / 16; ++j) {
           const int row = rbase + 16 * j;
-          const int cr = tok_lo + row;  // row within the chunk
-          const int rr = cr < tl.ntok ? cr : 0;
+          const int rr = row < tl.ntok ? row : 0;
           int tok = 0;
-          if (row < tok_n) {
+          if (row < tl.N) {
             if (tl.shared) {
               tok = tl.row0 + rr;
             } else {
@@ -500,28 +432,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         const uint32_t bs = t_smem(ts);
         if (tl.phase == 0) {
 #pragma unroll
-          for (int j = 0; j < L::kTokRows / 16; ++j) {
+          for (int j = 0; j < BN / 16; ++j) {
             const int row = rbase + 16 * j;
-            if (row < tok_n) cp_async_16(bs + row * 128 + ((c8 ^ (row & 7)) << 4), src[j] + k0);
+            if (row < tl.N) cp_async_16(bs + row * 128 + ((c8 ^ (row & 7)) << 4), src[j] + k0);
           }
           cp_async_arrive_noinc(tfull_bar(ts));
         } else if (tid == 0) {
-          // activation rows row0 + tok_lo + [0, tok_n) (contiguous, tok_n a
-          // multiple of 16): boxes of 128 rows while they fit, then 64/32/16
-          mbar_arrive_expect_tx(tfull_bar(ts), (uint32_t)(tok_n * 128));
+          // activation rows row0 .. row0 + N (contiguous, N a multiple of 16 and
+          // <= 256): boxes of 128 rows while they fit, then one each of 64/32/16
+          mbar_arrive_expect_tx(tfull_bar(ts), (uint32_t)(tl.N * 128));
           issued |= 1u << ts;
           issued_par = (issued_par & ~(1u << ts)) | (tph << ts);
           const CUtensorMap *mb = tl.shared ? p.map_acts : p.map_act;
           int off = 0;
-          while (tok_n - off >= 128) {
-            tma_load_2d(bs + (uint32_t)off * 128, &mb[3], tfull_bar(ts), k0, tl.row0 + tok_lo + off);
+          while (tl.N - off >= 128) {
+            tma_load_2d(bs + (uint32_t)off * 128, &mb[3], tfull_bar(ts), k0, tl.row0 + off);
             off += 128;
           }
 #pragma unroll
           for (int bi = 2; bi >= 0; --bi) {
             const int h = 16 << bi;
-            if (tok_n - off >= h) {
-              tma_load_2d(bs + (uint32_t)off * 128, &mb[bi], tfull_bar(ts), k0, tl.row0 + tok_lo + off);
+            if (tl.N - off >= h) {
+              tma_load_2d(bs + (uint32_t)off * 128, &mb[bi], tfull_bar(ts), k0, tl.row0 + off);
               off += h;
             }
           }
@@ -541,19 +473,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
           if ((issued >> s) & 1u) mbar_wait_drain(tfull_bar(s), (issued_par >> s) & 1u);
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0 && rank == 0) {
-      // ================= MMA issuer (a pair's first CTA issues for both)
+    // ================= MMA issuer
+    if (lane == 0) {
       int ws = 0, ts = 0;
       uint32_t wph = 0, tph = 0;
       bool any = false;
       for (int i = 0; ok; ++i) {
         const int r = i % kRing;
-        ok = wait_id(r, (uint32_t)(i / kRing) & 1u);
+        ok = mbar_wait(id_full(r), (uint32_t)(i / kRing) & 1u, err, abort_flag);
         if (!ok) break;
         const int t = ring[r];
-        release_id(r);
+        mbar_arrive(id_empty(r));
         if (t < 0) break;
-        const Tile tl = decode_tile<BN, PAIR>(p, t, start1, start2, seg_off, nseg);
+        const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
         const int acc = i % L::kAccBufs;
         const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
         ok = mbar_wait(aempty_bar(acc), aph ^ 1u, err, abort_flag);
@@ -561,13 +493,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         tc_fence_after();
         const uint32_t d0 = tmem + (uint32_t)(acc * 2 * BN);
         const uint32_t d1 = d0 + (uint32_t)BN;
-        const uint32_t idesc = idesc_bf16(PAIR ? 256 : 128, tl.N);
+        const uint32_t idesc = idesc_bf16(128, tl.N);
         for (int kb = 0; kb < tl.nk; ++kb) {
           ok = mbar_wait(wfull_bar(ws), wph, err, abort_flag) && mbar_wait(tfull_bar(ts), tph, err, abort_flag);
-          if (PAIR && ok) {  // the partner's slots of this K step (its relay signals 4 bytes)
-            mbar_arrive_expect_tx(pfull_bar(ts), 4u);
-            ok = mbar_wait_cluster(pfull_bar(ts), tph, err, abort_flag);
-          }
           if (!ok) break;
           if (tl.phase == 0) fence_proxy_async_smem();  // token rows were written by cp.async
           tc_fence_after();
@@ -577,22 +505,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-            if constexpr (PAIR) {
-              umma_bf16_pair(d0, a0 + 2 * kk, bd + 2 * kk, idesc, accum);
-              umma_bf16_pair(d1, a1 + 2 * kk, bd + 2 * kk, idesc, accum);
-            } else {
-              umma_bf16(d0, a0 + 2 * kk, bd + 2 * kk, idesc, accum);
-              umma_bf16(d1, a1 + 2 * kk, bd + 2 * kk, idesc, accum);
-            }
+            umma_bf16(d0, a0 + 2 * kk, bd + 2 * kk, idesc, accum);
+            umma_bf16(d1, a1 + 2 * kk, bd + 2 * kk, idesc, accum);
           }
           any = true;
-          if constexpr (PAIR) {  // release the slots of both CTAs
-            umma_commit_pair_mc(wempty_bar(ws), kBoth);
-            umma_commit_pair_mc(tempty_bar(ts), kBoth);
-          } else {
-            umma_commit(wempty_bar(ws));
-            umma_commit(tempty_bar(ts));
-          }
+          umma_commit(wempty_bar(ws));
+          umma_commit(tempty_bar(ts));
           if (++ws == KW) {
             ws = 0;
             wph ^= 1u;
@@ -603,71 +521,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
           }
         }
         if (!ok) break;
-        if constexpr (PAIR) umma_commit_pair_mc(afull_bar(acc), kBoth);
-        else umma_commit(afull_bar(acc));
+        umma_commit(afull_bar(acc));
       }
       if (!ok && any) {
-        if constexpr (PAIR) umma_commit_pair_mc(drain_bar, 1);
-        else umma_commit(drain_bar);
+        umma_commit(drain_bar);
         mbar_wait_drain(drain_bar, 0);
-      }
-    } else if (PAIR && lane == 0) {
-      // ================= the pair's second CTA: relay "my slots of K step q
-      // are full" to the first CTA's MMA thread
-      int ws = 0, ts = 0;
-      uint32_t wph = 0, tph = 0;
-      for (int i = 0; ok; ++i) {
-        const int r = i % kRing;
-        ok = wait_id(r, (uint32_t)(i / kRing) & 1u);
-        if (!ok) break;
-        const int t = ring[r];
-        release_id(r);
-        if (t < 0) break;
-        const Tile tl = decode_tile<BN, PAIR>(p, t, start1, start2, seg_off, nseg);
-        for (int kb = 0; kb < tl.nk; ++kb) {
-          ok = mbar_wait(wfull_bar(ws), wph, err, abort_flag) && mbar_wait(tfull_bar(ts), tph, err, abort_flag);
-          if (!ok) break;
-          fence_proxy_async_smem();  // token rows written by cp.async, read by the partner's MMAs
-          st_async_signal(map_cluster(smem_u32(relay_word + ts), 0), (uint32_t)kb, map_cluster(pfull_bar(ts), 0));
-          if (++ws == KW) {
-            ws = 0;
-            wph ^= 1u;
-          }
-          if (++ts == KT) {
-            ts = 0;
-            tph ^= 1u;
-          }
-        }
       }
     }
   } else {
     // ================= epilogue (warps 6..13 -> TMEM lane quarters 2,3,0,1, twice)
     const int q = warp & 3;
     // column groups of kEpiCols (32 for wide tiles: one TMEM wait per 32 columns);
-    // the lane quarter's warps take groups in turn
+    // the two warps of a lane quarter take alternate groups
     constexpr int kEpiCols = BN >= 64 ? kWideEpiCols : 16;
-    constexpr int kEpiStep = kEpiCols * (kEpiWarps / 4);
+    constexpr int kEpiStep = kEpiCols * (kEpiWarps / 4);  // the lane quarter's warps take groups in turn
     const int c_first = kEpiCols * ((warp - kEpiWarp0) >> 2);
     __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(smem + L::kEpiOff + (warp - kEpiWarp0) * kEpiCols * 64);
-    const int r = 32 * q + lane;  // TMEM lane = this CTA's weight row within a 128-row block
+    const int r = 32 * q + lane;  // weight row within the 128-row half
     for (int i = 0; ok; ++i) {
       const int rs = i % kRing;
-      ok = __all_sync(0xffffffffu, wait_id(rs, (uint32_t)(i / kRing) & 1u));
+      ok = __all_sync(0xffffffffu, mbar_wait(id_full(rs), (uint32_t)(i / kRing) & 1u, err, abort_flag));
       if (!ok) break;
       const int t = ring[rs];
       __syncwarp();
-      if (lane == 0) release_id(rs);
+      if (lane == 0) mbar_arrive(id_empty(rs));
       if (t < 0) break;
-      const Tile tl = decode_tile<BN, PAIR>(p, t, start1, start2, seg_off, nseg);
+      const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
       const int acc = i % L::kAccBufs;
       const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
       ok = __all_sync(0xffffffffu, mbar_wait(afull_bar(acc), aph, err, abort_flag));
       if (!ok) break;
       tc_fence_after();
       const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * 2 * BN);
-      // first weight row of this CTA's D0 / D1 blocks
-      const int row_a = tl.rb * tile_rows<PAIR>(tl.phase) + rank * 128;
-      const int row_b = row_a + tile_rows<PAIR>(tl.phase) / 2;
       if constexpr (L::kStageEpi) {
         // lane j of the warp owns weight row first + j; a group of ncol tokens is
         // written to the staging block as [token][32 rows] bf16, then each lane
@@ -685,7 +570,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         if (tl.phase == 0) {
           const int ld = tl.shared ? p.Is : p.I;
           __nv_bfloat16 *rows = (tl.shared ? p.act_s : p.act) + (size_t)tl.row0 * ld;
-          const int first = row_a + 32 * q;
+          const int first = tl.rb * 128 + 32 * q;
           for (int c = c_first; c < tl.N; c += kEpiStep) {
             float g[32], u[32];
             const int ncol = min(kEpiCols, tl.N - c);
@@ -704,6 +589,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
           }
         } else {
           __nv_bfloat16 *rows = (tl.shared ? p.y_s : p.y) + (size_t)tl.row0 * p.H;
+          const int first = tl.rb * 256 + 32 * q;
           for (int c = c_first; c < tl.N; c += kEpiStep) {
             float va[32], vb[32];
             const int ncol = min(kEpiCols, tl.N - c);
@@ -718,46 +604,74 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (j < ncol) stage[j * 32 + lane] = __float2bfloat16_rn(va[j]);
-            flush(rows, (size_t)p.H, row_a + 32 * q, p.H, c, ncol);
+            flush(rows, (size_t)p.H, first, p.H, c, ncol);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (j < ncol) stage[j * 32 + lane] = __float2bfloat16_rn(vb[j]);
-            flush(rows, (size_t)p.H, row_b + 32 * q, p.H, c, ncol);
+            flush(rows, (size_t)p.H, first + 128, p.H, c, ncol);
           }
         }
       } else if (tl.phase == 0) {
         const int ld = tl.shared ? p.Is : p.I;
         __nv_bfloat16 *out = tl.shared ? p.act_s : p.act;
-        const int ii = row_a + r;
+        const int ii = tl.rb * 128 + r;
         for (int c = c_first; c < tl.N; c += kEpiStep) {
-          for (int c16 = c; c16 < min(c + kEpiCols, tl.N); c16 += 16) {
-            float g[16], u[16];
-            tmem_ld16(t0 + (uint32_t)c16, g);
-            tmem_ld16(t0 + (uint32_t)(BN + c16), u);
+          if (kEpiCols == 32 && c + 32 <= tl.N) {
+            float g[32], u[32];
+            tmem_ld32(t0 + (uint32_t)c, g);
+            tmem_ld32(t0 + (uint32_t)(BN + c), u);
             tmem_wait_ld();
             if (ii < ld) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (c16 + j < tl.ntok)
-                  out[(size_t)(tl.row0 + c16 + j) * ld + ii] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
+              for (int j = 0; j < 32; ++j)
+                if (c + j < tl.ntok)
+                  out[(size_t)(tl.row0 + c + j) * ld + ii] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
+            }
+          } else {
+            for (int c16 = c; c16 < min(c + kEpiCols, tl.N); c16 += 16) {
+              float g[16], u[16];
+              tmem_ld16(t0 + (uint32_t)c16, g);
+              tmem_ld16(t0 + (uint32_t)(BN + c16), u);
+              tmem_wait_ld();
+              if (ii < ld) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (c16 + j < tl.ntok)
+                    out[(size_t)(tl.row0 + c16 + j) * ld + ii] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
+              }
             }
           }
         }
       } else {
         __nv_bfloat16 *out = tl.shared ? p.y_s : p.y;
-        const int ha = row_a + r, hb = row_b + r;
+        const int ha = tl.rb * 256 + r, hb = ha + 128;
         for (int c = c_first; c < tl.N; c += kEpiStep) {
-          for (int c16 = c; c16 < min(c + kEpiCols, tl.N); c16 += 16) {
-            float va[16], vb[16];
-            tmem_ld16(t0 + (uint32_t)c16, va);
-            tmem_ld16(t0 + (uint32_t)(BN + c16), vb);
+          if (kEpiCols == 32 && c + 32 <= tl.N) {
+            float va[32], vb[32];
+            tmem_ld32(t0 + (uint32_t)c, va);
+            tmem_ld32(t0 + (uint32_t)(BN + c), vb);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (c16 + j < tl.ntok) {
-                __nv_bfloat16 *row = out + (size_t)(tl.row0 + c16 + j) * p.H;
+            for (int j = 0; j < 32; ++j) {
+              if (c + j < tl.ntok) {
+                __nv_bfloat16 *row = out + (size_t)(tl.row0 + c + j) * p.H;
                 if (ha < p.H) row[ha] = __float2bfloat16_rn(va[j]);
                 if (hb < p.H) row[hb] = __float2bfloat16_rn(vb[j]);
+              }
+            }
+          } else {
+            for (int c16 = c; c16 < min(c + kEpiCols, tl.N); c16 += 16) {
+              float va[16], vb[16];
+              tmem_ld16(t0 + (uint32_t)c16, va);
+              tmem_ld16(t0 + (uint32_t)(BN + c16), vb);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (c16 + j < tl.ntok) {
+                  __nv_bfloat16 *row = out + (size_t)(tl.row0 + c16 + j) * p.H;
+                  if (ha < p.H) row[ha] = __float2bfloat16_rn(va[j]);
+                  if (hb < p.H) row[hb] = __float2bfloat16_rn(vb[j]);
+                }
               }
             }
           }
@@ -765,12 +679,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {  // release the accumulator (a pair's live in both CTAs; its MMA thread is in the first)
-        if (PAIR && rank != 0) mbar_arrive_cluster(map_cluster(aempty_bar(acc), 0));
-        else mbar_arrive(aempty_bar(acc));
-      }
+      if (lane == 0) mbar_arrive(aempty_bar(acc));
       if (tl.phase == 0 && (p.phases & 2)) {
-        // publish: this CTA's share of the gate/up tile is written (release to the down tiles)
+        // publish: this gate/up tile's activations are written (release to the down tiles)
         __threadfence();
         named_bar_sync(2, 32 * kEpiWarps);
         if (warp == kEpiWarp0 && lane == 0) atomicAdd(done1 + tl.seg, 1u);
@@ -780,13 +691,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
 
   __syncwarp();
   __syncthreads();
-  // a pair frees its TMEM together, and neither CTA leaves while the other may
-  // still signal its barriers
-  if constexpr (PAIR) cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    if constexpr (PAIR) tmem_dealloc_pair(tmem, L::kTmemCols);
-    else tmem_dealloc(tmem, L::kTmemCols);
+    tmem_dealloc(tmem, L::kTmemCols);
   }
   // the last CTA out zeroes the claim counter and the completion counts
   if (threadIdx.x == 0) {
@@ -811,35 +718,31 @@ int gemm_tile_n(int T) {
 }
 
 namespace {
-template <int BN, bool PAIR>
+template <int BN>
 cudaError_t launch_one(const GemmParams &p, int num_ctas, cudaStream_t stream, bool pdl) {
-  using L = Layout<BN, PAIR>;
+  using L = Layout<BN>;
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(expert_ffn_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(expert_ffn_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
   void *args[] = {(void *)&p};
-  const int ctas = PAIR ? num_ctas & ~1 : num_ctas;
-  return launch_ex((const void *)expert_ffn_kernel<BN, PAIR>, dim3(ctas), dim3(kGemmThreads), L::kSmem, stream, pdl,
-                   PAIR ? 2 : 1, args);
+  return launch_ex((const void *)expert_ffn_kernel<BN>, dim3(num_ctas), dim3(kGemmThreads), L::kSmem, stream, pdl, 1,
+                   args);
 }
 }  // namespace
 
-// 256-token tiles run on CTA pairs (clusters of two, 2-SM MMA); the narrow
-// tiles of small batches run one CTA per tile.
 cudaError_t launch_expert_ffn(const GemmParams &p, int bn, int num_ctas, cudaStream_t stream, bool pdl) {
   switch (bn) {
-    case 16: return launch_one<16, false>(p, num_ctas, stream, pdl);
-    case 32: return launch_one<32, false>(p, num_ctas, stream, pdl);
-    case 64: return launch_one<64, false>(p, num_ctas, stream, pdl);
-    case 128: return launch_one<128, false>(p, num_ctas, stream, pdl);
-    case 256: return num_ctas >= 2 ? launch_one<256, true>(p, num_ctas, stream, pdl)
-                                   : launch_one<256, false>(p, num_ctas, stream, pdl);
+    case 16: return launch_one<16>(p, num_ctas, stream, pdl);
+    case 32: return launch_one<32>(p, num_ctas, stream, pdl);
+    case 64: return launch_one<64>(p, num_ctas, stream, pdl);
+    case 128: return launch_one<128>(p, num_ctas, stream, pdl);
+    case 256: return launch_one<256>(p, num_ctas, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

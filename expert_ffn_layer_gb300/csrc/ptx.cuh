@@ -122,18 +122,6 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-// The same three for a CTA pair (2-SM MMA): issued by one warp in each CTA of
-// the pair, they allocate / release / free the same columns in both.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -166,26 +154,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
-}
-// 2-SM MMA, issued by one thread of the pair's first CTA: A is M = 256 rows,
-// 128 from each CTA's shared memory at the descriptor's offset; B's N rows are
-// split in halves, the first CTA's first; each CTA's TMEM receives its 128
-// rows x N columns of D.
-__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                               uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
-          d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive once on the barrier at `bar`'s offset in every CTA of `mask` when the
-// pair MMAs issued so far have completed.
-__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(mask)
-               : "memory");
 }
 // Arrive once on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -253,50 +221,6 @@ __device__ __forceinline__ uint32_t map_cluster(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
-}
-// Arrive on a barrier in another CTA of the cluster (address from map_cluster),
-// releasing this thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
-}
-// Asynchronous 4-byte store into another CTA's shared memory that also counts
-// 4 bytes of transaction on the barrier `remote_bar` there (both addresses from
-// map_cluster): a signal that does not wait for the remote side.
-__device__ __forceinline__ void st_async_signal(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(remote_addr), "r"(v),
-               "r"(remote_bar)
-               : "memory");
-}
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-// try_wait with acquire at cluster scope: for phases completed by another CTA's
-// arrivals that release its writes to this CTA's shared memory.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
-      "p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned *err,
-                                                  volatile int *abort_flag) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (abort_flag != nullptr && *abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        if (err != nullptr) atomicOr(err, MOE_DEVERR_TIMEOUT);
-        if (abort_flag != nullptr) *abort_flag = 1;
-        return false;
-      }
-    }
-  }
 }
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
   float v;
