@@ -10,8 +10,10 @@ weights resident in HBM.  The headline workload is the Hy3 decode batch
 (T = 8 tokens, H = 4096, 192 routed experts top-8 + 1 shared, I = 1536); the
 Hy3 prefill chunk (T = 4096) is measured too and reported in "prefill".
 
-L2 is flushed (a 256 MiB write) between timed steps; each step is timed with
-CUDA events on the launching stream.  Under torchrun each rank runs its own
+L2 is flushed between timed steps: a 256 MiB write, then a 256 MiB read of
+another buffer, so that the write-back of the flush's dirty lines is over
+before the step starts (left to the step it cost ~20 us of HBM time at
+decode); each step is timed with CUDA events on the launching stream.  Under torchrun each rank runs its own
 replica on its own tokens (weak scaling, no collective on the data path) and
 the slowest rank's time is used.
 
@@ -240,6 +242,13 @@ def run_ours(args, rank, world, local_rank):
         return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2(i):
+        """Evict L2: write a buffer larger than L2, then read another one, so that
+        L2 holds clean unrelated lines (no write-back left for the timed step)."""
+        flush.fill_(i & 0xFF)
+        flush_rd.sum()
 
     def setup(name, replica_seed):
         w = W.WORKLOADS[name]
@@ -262,7 +271,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         for i in range(K):
-            flush.fill_(i & 0xFF)
+            flush_l2(i)
             ev[i][0].record()
             fn()
             ev[i][1].record()
@@ -315,7 +324,7 @@ def run_ours(args, rank, world, local_rank):
         for name, fn in calls.items():
             g = graph_of(fn, K)
             g.replay()
-            flush.fill_(1)
+            flush_l2(1)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             g.replay()
@@ -393,7 +402,7 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) hidden, N(0,0.02) bf16 expert weights, N(0,0.02) fp32 router, "
                 "N(0,0.1) expert bias (the pages' shapes; no trained weights)",
-        "config": {**w.describe(), "workload": f"hy3_{name}_T{w.T}", "l2": "flushed between steps (256 MiB write)",
+        "config": {**w.describe(), "workload": f"hy3_{name}_T{w.T}", "l2": "flushed between steps (256 MiB write, then 256 MiB read of another buffer)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": f"CUDA graph of one layer forward ({layer_launches(w.T, w.top_k)} kernels, PDL-chained)",
                    "eager_ms_per_step": round(eager_ms / args.steps, 5),

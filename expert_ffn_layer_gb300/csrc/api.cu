@@ -252,7 +252,7 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
     }
   }
   if (!ok) return MOE_ERR_CUDA;
-  return cuda_status(launch_expert_ffn(g, gemm_tile_n(d.T), num_sms(), stream, pdl));
+  return cuda_status(launch_expert_ffn(g, gemm_tile_n(d.T, d.top_k, d.E), num_sms(), stream, pdl));
 }
 
 // a5-a6: gate/up GEMM through the route index + SiLU(gate) * up -> activations in ws

@@ -14,6 +14,7 @@ namespace moe {
 
 namespace {
 constexpr int kThreads = 256;
+constexpr int kMaxK = 16;  // top_k limit of the ABI
 
 __device__ __forceinline__ void acc8(float (&a)[8], const uint4 &v, float w) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -25,6 +26,10 @@ __device__ __forceinline__ void acc8(float (&a)[8], const uint4 &v, float w) {
 }
 }  // namespace
 
+// BATCHED: every slot's loads in flight at once (latency-bound small batches;
+// the register cost halves residency, which large, bandwidth-bound batches
+// need more), else one slot at a time.  Both add in slot order.
+template <bool BATCHED>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -35,16 +40,36 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     const int t = (int)(idx / hv);
     const int c = (int)(idx - (long long)t * hv);
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < p.top_k; ++j) {
-      int pos = __ldg(p.inv + (size_t)t * p.top_k + j);
-      pos = min(max(pos, 0), p.S - 1);
-      const float w = __ldg(p.topk_w + (size_t)t * p.top_k + j);
-      const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p.y_sorted + (size_t)pos * p.H) + c);
-      acc8(a, v, w);
-    }
-    if (p.y_shared != nullptr) {
-      const uint4 z = __ldcs(reinterpret_cast<const uint4 *>(p.y_shared + (size_t)t * p.H) + c);
-      acc8(a, z, 1.0f);
+    if constexpr (!BATCHED) {
+      for (int j = 0; j < p.top_k; ++j) {
+        const int pos = min(max(__ldg(p.inv + (size_t)t * p.top_k + j), 0), p.S - 1);
+        const float w = __ldg(p.topk_w + (size_t)t * p.top_k + j);
+        acc8(a, __ldcs(reinterpret_cast<const uint4 *>(p.y_sorted + (size_t)pos * p.H) + c), w);
+      }
+      if (p.y_shared != nullptr)
+        acc8(a, __ldcs(reinterpret_cast<const uint4 *>(p.y_shared + (size_t)t * p.H) + c), 1.0f);
+    } else {
+      // every slot's index and weight, then every row piece, in flight at once
+      // (top_k <= 16); accumulated in slot order
+      int pos[kMaxK];
+      float wt[kMaxK];
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < p.top_k) {
+          pos[j] = min(max(__ldg(p.inv + (size_t)t * p.top_k + j), 0), p.S - 1);
+          wt[j] = __ldg(p.topk_w + (size_t)t * p.top_k + j);
+        }
+      }
+      uint4 v[kMaxK];
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < p.top_k) v[j] = __ldcs(reinterpret_cast<const uint4 *>(p.y_sorted + (size_t)pos[j] * p.H) + c);
+      uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      if (p.y_shared != nullptr) z = __ldcs(reinterpret_cast<const uint4 *>(p.y_shared + (size_t)t * p.H) + c);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < p.top_k) acc8(a, v[j], wt[j]);
+      if (p.y_shared != nullptr) acc8(a, z, 1.0f);
     }
     uint4 o;
     uint32_t *ou = reinterpret_cast<uint32_t *>(&o);
@@ -71,7 +96,9 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream, bool pdl
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   void *args[] = {(void *)&p};
-  return launch_ex((const void *)combine_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, pdl, 1, args);
+  const bool batched = total <= (long long)nsm * kThreads;  // one wave of threads
+  return launch_ex(batched ? (const void *)combine_kernel<true> : (const void *)combine_kernel<false>,
+                   dim3((unsigned)blocks), dim3(kThreads), 0, stream, pdl, 1, args);
 }
 
 }  // namespace moe

@@ -41,8 +41,9 @@
 // (both 128-row boxes of one 64-wide K step, 32 KB) and kT token slots (N rows
 // of one K step), each with full/empty barriers; the MMA of K step q takes
 // weight slot q % kW and token slot q % kT.  Narrow tiles (decode) get six
-// weight slots -- as many weight bytes in flight per SM as HBM needs -- while
-// 256-token tiles keep three of each (fewer token slots starve the MMA).
+// weight slots -- as many weight bytes in flight per SM as HBM needs -- 240-
+// token tiles four, 256-token tiles three (fewer than three token slots
+// starve the MMA).
 //
 // Warp roles: 0 (one thread) claims tiles and issues the weight TMA loads; 1-4
 // load token rows (cp.async) or activation rows (TMA, one thread) and wait for
@@ -73,8 +74,8 @@ constexpr unsigned long long kDrainNs = 20000000ull;
 // Ring depths: weight slots of 32 KB and token slots of BN x 128 bytes.
 template <int BN>
 struct Rings {
-  static constexpr int kW = BN >= 256 ? 3 : BN >= 128 ? 5 : 6;
-  static constexpr int kT = BN >= 256 ? 3 : BN >= 64 ? 3 : 4;
+  static constexpr int kW = BN >= 256 ? 3 : BN >= 240 ? 4 : BN >= 128 ? 5 : 6;
+  static constexpr int kT = BN >= 64 ? 3 : 4;
 };
 
 template <int BN>
@@ -709,12 +710,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   }
 }
 
-int gemm_tile_n(int T) {
+// Widest tile for a batch.  Past 128 tokens: 256 when experts average more
+// than 256 tokens (fewer chunks, so fewer passes over each expert's weights),
+// else 240, whose smaller token slots leave room for a fourth weight slot --
+// more weight bytes in flight for the many one-chunk experts.
+int gemm_tile_n(int T, int top_k, int E) {
   if (T <= 16) return 16;
   if (T <= 32) return 32;
   if (T <= 64) return 64;
   if (T <= 128) return 128;
-  return 256;
+  return (long long)T * top_k > 256LL * E ? 256 : 240;
 }
 
 namespace {
@@ -742,6 +747,7 @@ cudaError_t launch_expert_ffn(const GemmParams &p, int bn, int num_ctas, cudaStr
     case 32: return launch_one<32>(p, num_ctas, stream, pdl);
     case 64: return launch_one<64>(p, num_ctas, stream, pdl);
     case 128: return launch_one<128>(p, num_ctas, stream, pdl);
+    case 240: return launch_one<240>(p, num_ctas, stream, pdl);
     case 256: return launch_one<256>(p, num_ctas, stream, pdl);
     default: return cudaErrorInvalidValue;
   }

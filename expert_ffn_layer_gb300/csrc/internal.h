@@ -75,7 +75,7 @@ struct GemmParams {
 // every launch leaves them zero again)
 constexpr int kSyncClaim = 64, kSyncExit = 65, kSyncPermute = 66, kSyncDone = 128;  // kSyncDone .. kSyncDone + 257
 constexpr int kWsHeaderBytes = 4096;
-int gemm_tile_n(int T);            // tokens per tile (multiple of 16, <= 256) chosen for a T
+int gemm_tile_n(int T, int top_k, int E);  // widest token tile (multiple of 16, <= 256) for a batch
 cudaError_t launch_expert_ffn(const GemmParams &p, int bn, int num_ctas, cudaStream_t stream, bool pdl);
 
 // --------------------------------------------------------------- combine

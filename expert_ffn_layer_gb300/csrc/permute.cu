@@ -6,8 +6,9 @@
 // output range per expert.  The HunyuanImage 3.0 post (Routed Experts) fixes
 // the slot numbering (flattened topk_idx) and the per-expert grouping.
 //
-// One CTA of 32 warps.  Warp w owns a contiguous run of slots.  Pass 1 counts
-// its run per expert in shared memory (warp match + popc); a column scan over
+// One CTA of 32 warps (8 for small batches).  Warp w owns a contiguous run of
+// slots.  Pass 1 counts its run per expert in shared memory (warp match +
+// popc); a column scan over
 // the warps and a scan over the experts give every (warp, expert) pair its
 // first output position; pass 2 walks the run again in slot order and ranks
 // equal experts inside a warp with match/popc, so the order inside every
@@ -26,13 +27,17 @@
 namespace moe {
 
 namespace {
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxE = 256;
+constexpr int kSmallS = 1024;  // up to this many slots the one-CTA kernel runs 8 warps
 constexpr int kUnroll = 8;
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1) permute_kernel(const PermuteParams p) {
+// One CTA of WARPS warps (32 for up to 8192 slots, 8 -- still one thread per
+// expert in the column scan -- for up to 1024).
+template <int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1) permute_kernel(const PermuteParams p) {
+  constexpr int kWarps = WARPS, kThreads = WARPS * 32;
+  static_assert(kThreads >= kMaxE, "one thread per expert in the column scan");
   __shared__ int base[kWarps][kMaxE];
   __shared__ int offs[kMaxE + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -309,7 +314,10 @@ __global__ void __launch_bounds__(kPartThreads) permute_scatter_kernel(const Per
 cudaError_t launch_permute(const PermuteParams &p, cudaStream_t stream, bool pdl) {
   void *args[] = {(void *)&p};
   const int G = permute_parts(p.S);
-  if (G == 0) return launch_ex((const void *)permute_kernel, dim3(1), dim3(kThreads), 0, stream, pdl, 1, args);
+  if (G == 0) {
+    if (p.S <= kSmallS) return launch_ex((const void *)permute_kernel<8>, dim3(1), dim3(256), 0, stream, pdl, 1, args);
+    return launch_ex((const void *)permute_kernel<32>, dim3(1), dim3(1024), 0, stream, pdl, 1, args);
+  }
   cudaError_t e = launch_ex((const void *)permute_count_kernel, dim3(G), dim3(kPartThreads), 0, stream, pdl, 1, args);
   if (e != cudaSuccess) return e;
   return launch_ex((const void *)permute_scatter_kernel, dim3(G), dim3(kPartThreads), 0, stream, pdl, 1, args);

@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_gemm_kernel(const __
 }
 
 // ------------------------------------------------------------------ topk
-// One CTA (256 threads) per token: thread e sums the KS partial logits of
-// expert e in slice order; warp 0 scores and selects.
+// One CTA (256 threads) per token: thread e sums the KS (<= 32) partial logits
+// of expert e in slice order; warp 0 scores and selects.
 __global__ void __launch_bounds__(256) router_topk_kernel(const __grid_constant__ RouterParams p, int KS) {
   __shared__ float lg[256];
   const int t = blockIdx.x;
@@ -213,19 +213,16 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const __grid_constant_
   pdl_wait();  // the partial logits come from the gemm kernel
   pdl_launch_dependents();
   if (tid < E) {
-    float acc = 0.0f;
+    // every slice's partial in flight at once (KS <= 32), then added in slice order
     const float *src = p.partial + (size_t)t * E + tid;
     const size_t stride = (size_t)p.T * E;
-    int s = 0;
-    for (; s + 4 <= KS; s += 4) {  // four loads in flight, added in slice order
-      const float a = __ldcg(src + (size_t)s * stride), b = __ldcg(src + (size_t)(s + 1) * stride);
-      const float c = __ldcg(src + (size_t)(s + 2) * stride), d = __ldcg(src + (size_t)(s + 3) * stride);
-      acc += a;
-      acc += b;
-      acc += c;
-      acc += d;
-    }
-    for (; s < KS; ++s) acc += __ldcg(src + (size_t)s * stride);
+    float part[32];
+#pragma unroll
+    for (int s = 0; s < 32; ++s) part[s] = s < KS ? __ldcg(src + (size_t)s * stride) : 0.0f;
+    float acc = 0.0f;
+#pragma unroll
+    for (int s = 0; s < 32; ++s)
+      if (s < KS) acc += part[s];
     lg[tid] = acc;
     if (p.logits_out != nullptr) p.logits_out[(size_t)t * E + tid] = acc;
   }

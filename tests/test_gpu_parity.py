@@ -240,8 +240,8 @@ def test_expert_ffn_parity(w):
 
 @pytest.mark.parametrize("T", [700, 512])
 def test_expert_ffn_skewed_segments(T):
-    """One expert holding every token (several chunks; T = 512 gives chunks of exactly
-    256 tokens, the widest tile) and empty experts."""
+    """One expert holding every token (several chunks) and empty experts; these
+    batches average at most 256 tokens per expert, so they run the 240-token tiles."""
     w = MID.with_(name="mid_skew", T=T)
     inp = W.layer_inputs(w)
     topk = np.zeros((w.T, 2), dtype=np.int32)
@@ -255,6 +255,30 @@ def test_expert_ffn_skewed_segments(T):
     y, z = dl.expert_ffn(i32_dev(perm), i32_dev(offsets))
     torch.cuda.synchronize()
     assert_layer_close(host_f64(y), y_ref, "skewed y_sorted")
+
+
+def test_expert_ffn_widest_tiles():
+    """T * k > 256 * E selects the 256-token tiles: one expert of two chunks of
+    exactly 256 tokens, one of five chunks, one of three."""
+    w = MID.with_(name="mid_wide_tiles", T=1040)
+    assert w.T * w.top_k > 256 * w.E
+    inp = W.layer_inputs(w)
+    t = np.arange(w.T)
+    topk = np.zeros((w.T, 2), dtype=np.int32)
+    topk[:, 0] = 3
+    topk[:, 1] = np.where(t < 512, 6, 1)
+    counts, offsets = oracle.histogram_offsets(topk, w.E)
+    assert counts[6] == 512 and counts[3] == 1040
+    perm, inv = oracle.permutation(topk, w.E)
+    y_ref = oracle.expert_outputs_sorted(inp["hidden"], perm, offsets, w.top_k, inp["w_gate"], inp["w_up"],
+                                         inp["w_down"])
+    z_ref = oracle.shared_expert(inp["hidden"], inp["ws_gate"], inp["ws_up"], inp["ws_down"])
+    dl = DeviceLayer(w, inp)
+    y, z = dl.expert_ffn(i32_dev(perm), i32_dev(offsets))
+    torch.cuda.synchronize()
+    assert_layer_close(host_f64(y), y_ref, "widest tiles y_sorted")
+    assert_layer_close(host_f64(z), z_ref, "widest tiles y_shared")
+    assert moe.moe_ws_read_error(dl.ws) == 0
 
 
 def test_expert_ffn_odd_row_blocks_and_chunks():
