@@ -417,29 +417,45 @@ def run_ours(args, rank, world, local_rank):
     del layer, hidden, layer_graph
     torch.cuda.empty_cache()
 
-    # ---------------- prefill chunk (T = 4096), single GPU
-    if world == 1 and not args.no_prefill:
-        pw, pd, player, phidden, _, _ = setup("prefill", 0)
-        pout = torch.empty((pw.T, pw.H), dtype=torch.bfloat16, device=dev)
-        pgraph = graph_of(lambda: player(phidden, pout), 1)
-        pst = timed(pgraph.replay, args.steps, args.warmup)
-        pms = float(np.mean(pst))
-        pst_ms, pact, pcounts = stage_times(pw, pd, player, phidden, max(3, args.steps // 2))
-        pwork = stage_work(pw, pact)
-        flops = pwork["expert_ffn"]["flops"]
-        wbytes = (pact * 3 * pw.I + 3 * pw.I_shared) * pw.H * 2
-        pdom = max(("route", "permute", "expert_ffn", "combine"), key=pst_ms.get)
-        result["prefill"] = {
-            "workload": f"hy3_prefill_T{pw.T}", "value": round(pw.T / (pms * 1e-3), 1), "unit": UNIT,
-            "ms_per_step": round(pms, 5), "active_experts": pact, "max_tokens_per_expert": int(pcounts.max()),
-            "layer_tensor_frac": round(flops / (pms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
-            "layer_hbm_frac": round(wbytes / (pms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
-            "roofline": roofline_for(pdom, pwork, pst_ms[pdom], pk, pk_kind, f"prefill_T{pw.T}"),
-            "kernels": {n: round(v, 4) for n, v in pst_ms.items()},
-            "gpu_launches": layer_launches(pw.T, pw.top_k) * args.steps,
+    # ---------------- the larger configurations, single GPU: the Hy3 prefill
+    # chunk (T = 4096), the skewed long prefill (T = 16384) and the
+    # HunyuanImage-style softmax layer (T = 8192)
+    def big_layer(name):
+        bw, bd, blayer, bhidden, _, _ = setup(name, 0)
+        bout = torch.empty((bw.T, bw.H), dtype=torch.bfloat16, device=dev)
+        bgraph = graph_of(lambda: blayer(bhidden, bout), 1)
+        bst = timed(bgraph.replay, args.steps, args.warmup)
+        bms = float(np.mean(bst))
+        # clocks under this workload's load: one second of back-to-back layers
+        with ClockSampler(local_rank) as bclk:
+            for _ in range(max(1, int(1.0 / (bms * 1e-3)))):
+                bgraph.replay()
+            torch.cuda.synchronize()
+        bst_ms, bact, bcounts = stage_times(bw, bd, blayer, bhidden, max(3, args.steps // 2))
+        bwork = stage_work(bw, bact)
+        flops = bwork["expert_ffn"]["flops"]
+        wbytes = (bact * 3 * bw.I + 3 * bw.I_shared) * bw.H * 2
+        bdom = max(("route", "permute", "expert_ffn", "combine"), key=bst_ms.get)
+        res = {
+            "workload": f"{'hy3_' if name != 'image' else 'hunyuanimage_'}{name}_T{bw.T}",
+            "value": round(bw.T / (bms * 1e-3), 1), "unit": UNIT,
+            "ms_per_step": round(bms, 5), "active_experts": bact, "max_tokens_per_expert": int(bcounts.max()),
+            "layer_tensor_frac": round(flops / (bms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+            "layer_hbm_frac": round(wbytes / (bms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "roofline": roofline_for(bdom, bwork, bst_ms[bdom], pk, pk_kind, f"{name}_T{bw.T}"),
+            "kernels": {n: round(v, 4) for n, v in bst_ms.items()},
+            "gpu_launches": layer_launches(bw.T, bw.top_k) * args.steps,
+            "clocks_under_load": bclk.summary(),
         }
-        del player, phidden, pgraph
+        del blayer, bhidden, bgraph
         torch.cuda.empty_cache()
+        return res
+
+    if world == 1 and not args.no_prefill:
+        result["prefill"] = big_layer("prefill")
+    if world == 1 and not args.no_extra:
+        result["zipf"] = big_layer("zipf")
+        result["image"] = big_layer("image")
 
     # ---------------- the oracle on the host cores (rank 0 only, N = 1)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -539,6 +555,8 @@ def main():
     ap.add_argument("--profile", action="store_true",
                     help="only run warm-up layer forwards and one more (for hardware-counter captures)")
     ap.add_argument("--no-prefill", action="store_true", help="skip the T=4096 prefill measurement")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the skewed long-prefill (T=16384) and HunyuanImage (T=8192) measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()

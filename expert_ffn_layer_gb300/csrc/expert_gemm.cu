@@ -194,10 +194,25 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// SiLU(g) * u with the fast reciprocal-based division: the result is rounded
-// to bf16, far coarser than the division's few-ulp error, and for g < -87 the
-// denominator overflows and the quotient goes to zero, which is SiLU's limit.
-__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// SiLU(g) * u = g * u / (1 + e^-g) with one special-function operation per
+// element (the epilogue of a 256-token tile is bound by them): e^-g =
+// 2^(-g log2 e) by the hardware base-2 exponential (argument capped at 120 so
+// the denominator stays a normal float), then 1/d by Newton's iteration
+// r <- r (2 - d r) from a bit-pattern seed.  The seed K - bits(d) with
+// K = 0x7EF311C0 (the constant that minimises its worst relative error, 5.1 %,
+// over a binade) reaches 6.5e-6 after two steps; with the exponential's error
+// the result is within 9e-6 of SiLU(g) * u relative -- far below the bf16
+// rounding that follows.  For g < -83 the true value is below 1e-34.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  const float x = fminf(-1.4426950409f * g, 120.0f);
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x));
+  const float d = 1.0f + e;
+  float r = __int_as_float(0x7EF311C0 - __float_as_int(d));
+  r = r * fmaf(-d, r, 2.0f);
+  r = r * fmaf(-d, r, 2.0f);
+  return g * u * r;
+}
 
 }  // namespace
 
@@ -557,14 +572,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       if constexpr (L::kStageEpi) {
         // lane j of the warp owns weight row first + j; a group of ncol tokens is
         // written to the staging block as [token][32 rows] bf16, then each lane
-        // stores 16 bytes (8 rows of one token): 4 lanes per token row piece
-        auto flush = [&](__nv_bfloat16 *rows, size_t ld, int first, int limit, int c, int ncol) {
+        // stores 16 bytes (8 rows of one token): 4 lanes per token row piece.
+        // y goes out with the streaming (evict-first) hint: it is read only by
+        // the combine after this kernel, while the activations are re-read
+        // here by the down tiles and should stay in L2.
+        auto flush = [&](__nv_bfloat16 *rows, size_t ld, int first, int limit, int c, int ncol, bool stream) {
           __syncwarp();
           for (int pass = 0; pass < ncol / 8; ++pass) {
             const int jj = pass * 8 + (lane >> 2), qq = lane & 3;
             const uint4 v = *reinterpret_cast<const uint4 *>(stage + jj * 32 + qq * 8);
-            if (c + jj < tl.ntok && first + qq * 8 < limit)
-              *reinterpret_cast<uint4 *>(rows + (size_t)(c + jj) * ld + first + qq * 8) = v;
+            if (c + jj < tl.ntok && first + qq * 8 < limit) {
+              uint4 *dst = reinterpret_cast<uint4 *>(rows + (size_t)(c + jj) * ld + first + qq * 8);
+              if (stream) __stcs(dst, v);
+              else *dst = v;
+            }
           }
           __syncwarp();
         };
@@ -586,7 +607,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (j < ncol) stage[j * 32 + lane] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
-            flush(rows, (size_t)ld, first, ld, c, ncol);
+            flush(rows, (size_t)ld, first, ld, c, ncol, false);
           }
         } else {
           __nv_bfloat16 *rows = (tl.shared ? p.y_s : p.y) + (size_t)tl.row0 * p.H;
@@ -605,11 +626,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (j < ncol) stage[j * 32 + lane] = __float2bfloat16_rn(va[j]);
-            flush(rows, (size_t)p.H, first, p.H, c, ncol);
+            flush(rows, (size_t)p.H, first, p.H, c, ncol, true);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (j < ncol) stage[j * 32 + lane] = __float2bfloat16_rn(vb[j]);
-            flush(rows, (size_t)p.H, first + 128, p.H, c, ncol);
+            flush(rows, (size_t)p.H, first + 128, p.H, c, ncol, true);
           }
         }
       } else if (tl.phase == 0) {
@@ -656,8 +677,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
             for (int j = 0; j < 32; ++j) {
               if (c + j < tl.ntok) {
                 __nv_bfloat16 *row = out + (size_t)(tl.row0 + c + j) * p.H;
-                if (ha < p.H) row[ha] = __float2bfloat16_rn(va[j]);
-                if (hb < p.H) row[hb] = __float2bfloat16_rn(vb[j]);
+                if (ha < p.H) __stcs(row + ha, __float2bfloat16_rn(va[j]));
+                if (hb < p.H) __stcs(row + hb, __float2bfloat16_rn(vb[j]));
               }
             }
           } else {
@@ -670,8 +691,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
               for (int j = 0; j < 16; ++j) {
                 if (c16 + j < tl.ntok) {
                   __nv_bfloat16 *row = out + (size_t)(tl.row0 + c16 + j) * p.H;
-                  if (ha < p.H) row[ha] = __float2bfloat16_rn(va[j]);
-                  if (hb < p.H) row[hb] = __float2bfloat16_rn(vb[j]);
+                  if (ha < p.H) __stcs(row + ha, __float2bfloat16_rn(va[j]));
+                  if (hb < p.H) __stcs(row + hb, __float2bfloat16_rn(vb[j]));
                 }
               }
             }

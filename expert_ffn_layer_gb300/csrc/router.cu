@@ -203,32 +203,9 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_gemm_kernel(const __
 }
 
 // ------------------------------------------------------------------ topk
-// One CTA (256 threads) per token: thread e sums the KS (<= 32) partial logits
-// of expert e in slice order; warp 0 scores and selects.
-__global__ void __launch_bounds__(256) router_topk_kernel(const __grid_constant__ RouterParams p, int KS) {
-  __shared__ float lg[256];
-  const int t = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31;
+// Scoring and top-k selection of token t by one warp from its logits lg[0..E).
+__device__ __forceinline__ void select_topk(const RouterParams &p, const float *lg, int t, int lane) {
   const int E = p.E, k = p.top_k;
-  pdl_wait();  // the partial logits come from the gemm kernel
-  pdl_launch_dependents();
-  if (tid < E) {
-    // every slice's partial in flight at once (KS <= 32), then added in slice order
-    const float *src = p.partial + (size_t)t * E + tid;
-    const size_t stride = (size_t)p.T * E;
-    float part[32];
-#pragma unroll
-    for (int s = 0; s < 32; ++s) part[s] = s < KS ? __ldcg(src + (size_t)s * stride) : 0.0f;
-    float acc = 0.0f;
-#pragma unroll
-    for (int s = 0; s < 32; ++s)
-      if (s < KS) acc += part[s];
-    lg[tid] = acc;
-    if (p.logits_out != nullptr) p.logits_out[(size_t)t * E + tid] = acc;
-  }
-  __syncthreads();
-  if (tid >= 32) return;
-
   const int nj = (E + 31) >> 5;
   float v[8], key[8], sc[8];
 #pragma unroll
@@ -308,6 +285,49 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const __grid_constant_
   }
 }
 
+// TPC tokens per CTA (256 threads).  TPC = 1 (many K slices, small batches):
+// thread e sums the KS (<= 32) partial logits of expert e in slice order with
+// every load in flight (one round of latency); warp 0 selects.  TPC = 8 (at
+// most 4 slices, large batches): the CTA's threads sum the 8 x E logits, then
+// warp w selects for the CTA's token w -- all warps select, not one in eight.
+template <int TPC>
+__global__ void __launch_bounds__(256) router_topk_kernel(const __grid_constant__ RouterParams p, int KS) {
+  __shared__ float lg[TPC][256];
+  const int t0 = blockIdx.x * TPC;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = p.E;
+  pdl_wait();  // the partial logits come from the gemm kernel
+  pdl_launch_dependents();
+  const size_t stride = (size_t)p.T * E;
+  // this thread's (token, expert) pairs i = tid + 256 j; every partial of every
+  // pair in flight together, then each pair added in slice order
+  constexpr int kPairs = (TPC * 256 + 255) / 256;  // pairs per thread (E <= 256)
+  constexpr int kMaxKS = TPC == 1 ? 32 : 4;        // slices this form takes
+  float part[kPairs][kMaxKS];
+#pragma unroll
+  for (int j = 0; j < kPairs; ++j) {
+    const int i = tid + 256 * j, tok = i / E, e = i - tok * E;
+    const bool on = i < TPC * E && t0 + tok < p.T;
+    const float *src = p.partial + (size_t)(t0 + tok) * E + e;
+#pragma unroll
+    for (int s = 0; s < kMaxKS; ++s) part[j][s] = (on && s < KS) ? __ldcg(src + (size_t)s * stride) : 0.0f;
+  }
+#pragma unroll
+  for (int j = 0; j < kPairs; ++j) {
+    const int i = tid + 256 * j, tok = i / E, e = i - tok * E;
+    if (i < TPC * E && t0 + tok < p.T) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int s = 0; s < kMaxKS; ++s)
+        if (s < KS) acc += part[j][s];
+      lg[tok][e] = acc;
+      if (p.logits_out != nullptr) p.logits_out[(size_t)(t0 + tok) * E + e] = acc;
+    }
+  }
+  __syncthreads();
+  if (warp < TPC && t0 + warp < p.T) select_topk(p, lg[warp], t0 + warp, lane);
+}
+
 cudaError_t launch_router(const RouterParams &p, const float *router_w, int ksplit, int mtiles, cudaStream_t stream,
                           bool pdl) {
   static thread_local int configured_dev = -1, nsm = 0;
@@ -338,10 +358,11 @@ cudaError_t launch_router(const RouterParams &p, const float *router_w, int kspl
                               router_smem_bytes(p.Epad, p.stages), stream, true, 1, args);
     if (e != cudaSuccess) return e;
   }
-  {  // topk
+  {  // topk: one token per CTA for small batches, eight for large ones
     int ks = ksplit;
     void *args[] = {(void *)&p, (void *)&ks};
-    return launch_ex((const void *)router_topk_kernel, dim3(p.T), dim3(256), 0, stream, true, 1, args);
+    if (ksplit > 4) return launch_ex((const void *)router_topk_kernel<1>, dim3(p.T), dim3(256), 0, stream, true, 1, args);
+    return launch_ex((const void *)router_topk_kernel<8>, dim3((p.T + 7) / 8), dim3(256), 0, stream, true, 1, args);
   }
 }
 
