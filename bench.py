@@ -441,6 +441,9 @@ def run_ours(args, rank, world, local_rank):
             "value": round(bw.T / (bms * 1e-3), 1), "unit": UNIT,
             "ms_per_step": round(bms, 5), "active_experts": bact, "max_tokens_per_expert": int(bcounts.max()),
             "layer_tensor_frac": round(flops / (bms * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+            # the same against the sustained (power-capped, seconds-long) bf16 figure
+            "layer_tensor_frac_sustained": (round(flops / (bms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 4)
+                                            if pk.get("bf16_tflops_sustained") else None),
             "layer_hbm_frac": round(wbytes / (bms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
             "roofline": roofline_for(bdom, bwork, bst_ms[bdom], pk, pk_kind, f"{name}_T{bw.T}"),
             "kernels": {n: round(v, 4) for n, v in bst_ms.items()},
