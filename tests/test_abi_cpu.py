@@ -61,9 +61,11 @@ def test_workspace_bytes(lib):
     d = _hy3(4096)
     n = moe.moe_workspace_bytes(d)
     S = 4096 * 8
-    # dominated by y_sorted [S,H], y_shared [T,H], A_act [S,I], A_shared [T,I] (bf16)
+    # dominated by y_sorted [S,H], y_shared [T,H], A_act [S,I], A_shared [T,I]
+    # (bf16); the rest (routing tables, the router's bf16 weight halves and its
+    # split-K partial logits) is a few tens of MB
     core = 2 * (S * 4096 + 4096 * 4096 + S * 1536 + 4096 * 1536)
-    assert core <= n <= core + 1 << 20
+    assert core <= n <= core + (32 << 20)
     assert n % 256 == 0
     assert moe.moe_workspace_bytes(_hy3(8)) < n
     assert lib.moe_workspace_bytes(ctypes.byref(moe.dims(8, 4000, 192, 1536, 8))) == 0
