@@ -8,6 +8,7 @@ Function names follow the C ABI:
 
     moe_route, moe_permute, moe_expert_ffn (= moe_expert_gate_up + moe_expert_down),
     moe_combine, moe_layer_forward,
+    moe_fused_moe (routing given, stacked [E, 2I, H] gate/up weights),
     moe_workspace_bytes, moe_ws_init, moe_ws_read_error, moe_check_dims
 
 Tensors are torch tensors on the current CUDA device: bf16 activations and
@@ -31,7 +32,7 @@ SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
 
 EXPORTS = ("moe_status_string", "moe_check_dims", "moe_workspace_bytes", "moe_ws_init", "moe_ws_read_error",
            "moe_route", "moe_permute", "moe_expert_ffn", "moe_expert_gate_up", "moe_expert_down", "moe_combine",
-           "moe_layer_forward", "moe_expert_ffn_noalloc", "moe_selftest_wait_timeout")
+           "moe_layer_forward", "moe_fused_moe", "moe_expert_ffn_noalloc", "moe_selftest_wait_timeout")
 
 
 class MoeError(RuntimeError):
@@ -81,6 +82,7 @@ def load() -> ctypes.CDLL:
         "moe_expert_down": (st, [D, P, P, P, P, P, P, C, P]),
         "moe_combine": (st, [D, P, P, P, P, P, P]),
         "moe_layer_forward": (st, [D, P, P, P, P, P, P, P, P, P, P, P, C, P]),
+        "moe_fused_moe": (st, [D, P, P, P, P, P, P, P, P, P, C, P]),
         "moe_selftest_wait_timeout": (st, [P, C, ctypes.c_ulonglong, P]),
     }
     for name, (res, args) in sig.items():
@@ -241,6 +243,43 @@ def moe_layer_forward(d: MoeDims, hidden, router_w, expert_bias, w_gate, w_up, w
     _call("moe_layer_forward", ctypes.byref(d), _ptr(hidden), _ptr(router_w), _ptr(expert_bias), _ptr(w_gate),
           _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(out), _ptr(ws), ws.numel(),
           _stream(stream))
+
+
+def moe_fused_moe(d: MoeDims, hidden, topk_idx, topk_w, w_gate_up, w_down, ws_gate_up, ws_down, out, ws,
+                  stream=None) -> None:
+    _check(hidden, torch.bfloat16, (d.T, d.H), "hidden")
+    _check(topk_idx, torch.int32, (d.T, d.top_k), "topk_idx")
+    _check(topk_w, torch.float32, (d.T, d.top_k), "topk_w")
+    _check(w_gate_up, torch.bfloat16, (d.E, 2 * d.I, d.H), "w_gate_up")
+    _check(w_down, torch.bfloat16, (d.E, d.H, d.I), "w_down")
+    _check(out, torch.bfloat16, (d.T, d.H), "out")
+    if d.has_shared:
+        _check(ws_gate_up, torch.bfloat16, (2 * d.I_shared, d.H), "ws_gate_up")
+        _check(ws_down, torch.bfloat16, (d.H, d.I_shared), "ws_down")
+    _call("moe_fused_moe", ctypes.byref(d), _ptr(hidden), _ptr(topk_idx), _ptr(topk_w), _ptr(w_gate_up), _ptr(w_down),
+          _ptr(ws_gate_up), _ptr(ws_down), _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def fused_moe(hidden, topk_index, topk_weight, w_gate_up, w_down, output=None, ws_gate_up=None, ws_down=None,
+              workspace=None, stream=None):
+    """The fused-MoE call in the form the HunyuanImage 3.0 post shows it:
+    flattened tokens [T, H] bf16, top-k indices [T, k] int32 and weights [T, k]
+    fp32, stacked w_gate_up [E, 2I, H] (gate rows first) and w_down [E, H, I];
+    optional shared expert ws_gate_up [2 I_s, H], ws_down [H, I_s] (added
+    unweighted).  Returns `output` ([T, H] bf16, allocated when None)."""
+    T, H = hidden.shape
+    E, two_i, _ = w_gate_up.shape
+    k = topk_index.shape[1]
+    has_shared = ws_gate_up is not None
+    d = dims(T, H, E, two_i // 2, k, I_shared=(ws_gate_up.shape[0] // 2) if has_shared else 0,
+             score_mode="softmax", route_scale=1.0, has_shared=has_shared)
+    if output is None:
+        output = torch.empty((T, H), dtype=torch.bfloat16, device=hidden.device)
+    if workspace is None:
+        workspace = alloc_workspace(d, hidden.device)
+    moe_fused_moe(d, hidden, topk_index, topk_weight, w_gate_up, w_down, ws_gate_up, ws_down, output, workspace,
+                  stream)
+    return output
 
 
 def moe_selftest_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> None:

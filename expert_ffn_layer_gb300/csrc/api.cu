@@ -76,10 +76,12 @@ bool map_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, 
   const uint32_t box[2] = {64, box_rows};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-// stacked bf16 [n][rows][cols], box {64, box_rows, 1}, 128-byte swizzle
-bool map_bf16_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t n, uint32_t box_rows) {
+// stacked bf16 [n][rows][cols] (consecutive matrices `stride_rows` rows apart,
+// rows by default), box {64, box_rows, 1}, 128-byte swizzle
+bool map_bf16_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t n, uint32_t box_rows,
+                 uint64_t stride_rows = 0) {
   const uint64_t dims[3] = {cols, rows, n};
-  const uint64_t str[2] = {cols * 2, cols * rows * 2};
+  const uint64_t str[2] = {cols * 2, cols * (stride_rows ? stride_rows : rows) * 2};
   const uint32_t box[3] = {64, box_rows, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -210,12 +212,14 @@ moe_status do_permute(const moe_dims &d, const int32_t *topk_idx, int32_t *count
 }
 
 // Tensor maps and pointers of the grouped expert FFN; `phases` selects gate/up
-// (1), down (2) or both in one persistent launch (3).
+// (1), down (2) or both in one persistent launch (3).  gu_stride: rows from one
+// expert's gate (up) matrix to the next's -- I for separate [E, I, H] tensors,
+// 2I when w_gate and w_up point into one [E, 2I, H] tensor (up = gate + I rows).
 moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidden, const int32_t *perm,
                             const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
                             const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
                             const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws,
-                            cudaStream_t stream, bool pdl) {
+                            cudaStream_t stream, bool pdl, uint64_t gu_stride = 0) {
   const WsLayout L = ws_layout(d);
   GemmParams g;
   std::memset(&g, 0, sizeof(g));
@@ -239,7 +243,8 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
   g.y_s = reinterpret_cast<__nv_bfloat16 *>(y_shared);
   bool ok = true;
   if (phases & 1) {
-    ok = ok && map_bf16_3d(&g.map_wg, w_gate, d.H, d.I, d.E, 128) && map_bf16_3d(&g.map_wu, w_up, d.H, d.I, d.E, 128);
+    ok = ok && map_bf16_3d(&g.map_wg, w_gate, d.H, d.I, d.E, 128, gu_stride) &&
+         map_bf16_3d(&g.map_wu, w_up, d.H, d.I, d.E, 128, gu_stride);
     if (d.has_shared)
       ok = ok && map_bf16_2d(&g.map_sg, ws_gate, d.H, g.Is, 128) && map_bf16_2d(&g.map_su, ws_up, d.H, g.Is, 128);
   }
@@ -295,6 +300,24 @@ moe_status do_combine(const moe_dims &d, const moe_bf16 *y_sorted, const moe_bf1
 }
 
 bool ptr_ok(const void *p) { return p != nullptr && aligned16(p); }
+
+// Steps a3-a9 from a given routing, with the gate and up projections of every
+// expert stacked in one tensor: permutation, grouped expert FFN, combine.
+moe_status do_fused_moe(const moe_dims &d, const moe_bf16 *hidden, const int32_t *topk_idx, const float *topk_w,
+                        const moe_bf16 *w_gate_up, const moe_bf16 *w_down, const moe_bf16 *ws_gate_up,
+                        const moe_bf16 *ws_down, moe_bf16 *out, void *ws, cudaStream_t s) {
+  const WsLayout L = ws_layout(d);
+  int32_t *perm = at<int32_t>(ws, L.perm), *inv = at<int32_t>(ws, L.inv);
+  int32_t *offs = at<int32_t>(ws, L.offsets);
+  moe_bf16 *y = at<moe_bf16>(ws, L.y_sorted), *z = at<moe_bf16>(ws, L.y_shared);
+  moe_status st = do_permute(d, topk_idx, at<int32_t>(ws, L.counts), offs, perm, inv, ws, s, true);
+  if (st != MOE_OK) return st;
+  const size_t up = (size_t)d.I * d.H, sup = d.has_shared ? (size_t)d.I_shared * d.H : 0;
+  st = do_expert_phases(d, 3, hidden, perm, offs, w_gate_up, w_gate_up + up, w_down, ws_gate_up,
+                        d.has_shared ? ws_gate_up + sup : nullptr, ws_down, y, z, ws, s, true, 2 * (uint64_t)d.I);
+  if (st != MOE_OK) return st;
+  return do_combine(d, y, z, inv, topk_w, out, s, true);
+}
 
 }  // namespace
 }  // namespace moe
@@ -440,6 +463,22 @@ MOE_API moe_status moe_combine(const moe_dims *d, const moe_bf16 *y_sorted, cons
   if (!ptr_ok(y_sorted) || !ptr_ok(inv_perm) || !ptr_ok(topk_w) || !ptr_ok(out)) return MOE_ERR_INVALID_ARG;
   if (d->has_shared && !ptr_ok(y_shared)) return MOE_ERR_INVALID_ARG;
   return do_combine(*d, y_sorted, y_shared, inv_perm, topk_w, out, (cudaStream_t)stream, true);
+}
+
+MOE_API moe_status moe_fused_moe(const moe_dims *d, const moe_bf16 *hidden, const int32_t *topk_idx,
+                                 const float *topk_w, const moe_bf16 *w_gate_up, const moe_bf16 *w_down,
+                                 const moe_bf16 *ws_gate_up, const moe_bf16 *ws_down, moe_bf16 *out, void *ws,
+                                 size_t ws_bytes, void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(hidden) || !ptr_ok(topk_idx) || !ptr_ok(topk_w) || !ptr_ok(w_gate_up) || !ptr_ok(w_down) ||
+      !ptr_ok(out))
+    return MOE_ERR_INVALID_ARG;
+  if (d->has_shared && (!ptr_ok(ws_gate_up) || !ptr_ok(ws_down))) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  return do_fused_moe(*d, hidden, topk_idx, topk_w, w_gate_up, w_down, ws_gate_up, ws_down, out, ws,
+                      (cudaStream_t)stream);
 }
 
 MOE_API moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,

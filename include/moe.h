@@ -206,6 +206,29 @@ moe_status moe_expert_ffn_noalloc(const moe_dims *d, const moe_bf16 *hidden, con
 moe_status moe_combine(const moe_dims *d, const moe_bf16 *y_sorted, const moe_bf16 *y_shared,
                        const int32_t *inv_perm, const float *topk_w, moe_bf16 *out, void *stream);
 
+/* Steps a3-a9 from a given routing, with stacked fused gate/up weights: the
+ * shape of the fused-MoE call of [image] ("flashinfer" path: the flattened
+ * tokens, the top-k expert indices and routing weights, and the expert
+ * weights stacked along an expert dimension, [E, 2I, H] gate/up and
+ * [E, H, I] down, handed to one fused kernel chain).  Runs moe_permute,
+ * the grouped expert FFN and moe_combine on `stream`; intermediates in `ws`.
+ *   hidden      [T, H] bf16 (input)
+ *   topk_idx    [T, top_k] int32 expert of each slot, in [0, E) (input)
+ *   topk_w      [T, top_k] fp32 combine weight of each slot (input)
+ *   w_gate_up   [E, 2I, H] bf16: rows [0, I) of expert e are its gate
+ *               projection, rows [I, 2I) its up projection (input)
+ *   w_down      [E, H, I] bf16 (input)
+ *   ws_gate_up  [2 * I_shared, H] bf16, gate rows then up rows, and
+ *   ws_down     [H, I_shared] bf16: the shared expert (NULL when !has_shared)
+ *   out         [T, H] bf16 (output)
+ * The results equal moe_permute + moe_expert_ffn + moe_combine on the same
+ * weights held as separate w_gate / w_up tensors, bit for bit.  Errors as for
+ * moe_permute and moe_expert_ffn (an index outside [0, E) sets
+ * MOE_DEVERR_INDEX in the workspace error word). */
+moe_status moe_fused_moe(const moe_dims *d, const moe_bf16 *hidden, const int32_t *topk_idx, const float *topk_w,
+                         const moe_bf16 *w_gate_up, const moe_bf16 *w_down, const moe_bf16 *ws_gate_up,
+                         const moe_bf16 *ws_down, moe_bf16 *out, void *ws, size_t ws_bytes, void *stream);
+
 /* The whole layer (a1-a9) chained on `stream` with programmatic dependent
  * launch; every intermediate lives in `ws`.  Arguments as above; out [T, H] bf16. */
 moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,

@@ -80,6 +80,7 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
     assert lib.moe_expert_ffn(byref(d), *([None] * 12), 0, None) == 1
     assert lib.moe_combine(byref(d), None, None, None, None, None, None) == 1
     assert lib.moe_layer_forward(byref(d), *([None] * 11), 0, None) == 1
+    assert lib.moe_fused_moe(byref(d), *([None] * 9), 0, None) == 1
     # misaligned pointer (never dereferenced: validation fails first)
     bad = 0x1003
     assert lib.moe_combine(byref(d), bad, bad, bad, bad, bad, None) == 1

@@ -317,6 +317,43 @@ def test_expert_ffn_decode_shape():
     assert_layer_close(host_f64(z), ref["z"], "decode y_shared")
 
 
+# ------------------------------------------------------------------ stacked gate/up weights, routing given
+
+@pytest.mark.parametrize("w", [W.WORKLOADS["tiny"], MID_SOFTMAX, NOSHARED, W.WORKLOADS["decode"]],
+                         ids=["tiny", "mid_softmax", "noshared", "decode"])
+def test_fused_moe_stacked_gate_up(w):
+    """moe_fused_moe on [E, 2I, H] stacked gate/up weights (gate rows first)
+    equals permute + expert FFN + combine on the separate tensors bit for bit,
+    and matches the oracle's layer for the same routing."""
+    inp = inputs_of(w)
+    topk, wts = W.synthetic_topk(w, 3), W.synthetic_weights(w, 3)
+    # renormalised as routing makes them (sum route_scale), which keeps |out| in
+    # the range the layer tolerance is stated for
+    wts = (wts / wts.sum(axis=1, keepdims=True) * w.route_scale).astype(np.float32)
+    dl = DeviceLayer(w, inp)
+    idx, wt = i32_dev(topk), f32_dev(wts)
+    counts, offsets, perm, inv = dl.permute(idx)
+    y, z = dl.expert_ffn(perm, offsets)
+    staged = dl.combine(y, z, inv, wt)
+    gu = torch.cat([dl.w_gate, dl.w_up], dim=1).contiguous()
+    sgu = torch.cat([dl.ws_gate, dl.ws_up], dim=0).contiguous() if w.has_shared else None
+    out = torch.empty_like(staged)
+    moe.moe_fused_moe(dl.d, dl.hidden, idx, wt, gu, dl.w_down, sgu, dl.ws_down, out, dl.ws)
+    out2 = moe.fused_moe(dl.hidden, idx, wt, gu, dl.w_down, ws_gate_up=sgu, ws_down=dl.ws_down)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), staged.view(torch.int16))
+    assert torch.equal(out2.view(torch.int16), staged.view(torch.int16))
+    assert moe.moe_ws_read_error(dl.ws) == 0
+    _, offs_r = oracle.histogram_offsets(topk, w.E)
+    perm_r, inv_r = oracle.permutation(topk, w.E)
+    y_ref = oracle.expert_outputs_sorted(inp["hidden"], perm_r, offs_r, w.top_k, inp["w_gate"], inp["w_up"],
+                                         inp["w_down"])
+    z_ref = (oracle.shared_expert(inp["hidden"], inp["ws_gate"], inp["ws_up"], inp["ws_down"])
+             if w.has_shared else None)
+    ref = oracle.combine(y_ref, inv_r, wts.astype(np.float64), z_ref)
+    assert_layer_close(host_f64(out), ref, f"{w.name} fused_moe")
+
+
 # ------------------------------------------------------------------ combine
 
 @pytest.mark.parametrize("w", [W.WORKLOADS["tiny"], MID, W.WORKLOADS["decode"], NOSHARED],
