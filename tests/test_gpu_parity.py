@@ -107,6 +107,37 @@ def test_route_parity(w):
     _check_route(w, inp, dl)
 
 
+def _router_only(w):
+    """Device inputs of the router alone (no expert weights)."""
+    hidden, router_w, bias = W.router_inputs(w)
+    inp = {"hidden": hidden, "router_w": router_w, "bias": bias}
+    dl = type("R", (), {})()
+    dl.d = dims_of(w)
+    dl.hidden, dl.router_w, dl.bias = bf16_dev(hidden), f32_dev(router_w), f32_dev(bias)
+    dl.ws = moe.alloc_workspace(dl.d)
+    dl.route = lambda: DeviceLayer.route(dl)
+    return inp, dl
+
+
+@pytest.mark.parametrize("T,H,E,k,mode", [(128, 1024, 192, 8, "sigmoid"), (129, 1024, 192, 8, "sigmoid"),
+                                          (100, 512, 256, 8, "softmax"), (1, 4096, 192, 8, "sigmoid"),
+                                          (77, 640, 48, 6, "sigmoid")])
+def test_route_one_tile_and_boundary(T, H, E, k, mode):
+    """A full 128-token tile, one token more (a second tile of one row), a
+    single token, E = 256 (one 256-column accumulator pair), and H = 640 (ten K
+    slices: a split of two).  The router matches the oracle and repeats bit for
+    bit (the split-K partial logits are summed in a fixed order)."""
+    w = W.Workload(f"r{T}_{H}_{E}", T, H, E, k, 128, 128, mode, 2.826 if mode == "sigmoid" else 1.0,
+                   0.0 if mode == "sigmoid" else 1e-8, True, "normal" if mode == "sigmoid" else "none",
+                   0.1 if mode == "sigmoid" else 0.0, 21)
+    inp, dl = _router_only(w)
+    _check_route(w, inp, dl)
+    a_idx, a_w, a_lg = dl.route()
+    b_idx, b_w, b_lg = dl.route()
+    torch.cuda.synchronize()
+    assert torch.equal(a_idx, b_idx) and torch.equal(a_w, b_w) and torch.equal(a_lg, b_lg)
+
+
 @pytest.mark.parametrize("name,T", [("prefill", 4096), ("zipf", 16384), ("image", 8192), ("prefill_u", 4096)])
 def test_route_parity_full_size(name, T):
     """Router at the full workload sizes, every row (the oracle logits are one fp64 GEMM)."""
