@@ -48,8 +48,10 @@
 // Warp roles: 0 (one thread) claims tiles and issues the weight TMA loads; 1-4
 // load token rows (cp.async) or activation rows (TMA, one thread) and wait for
 // a down tile's gate/up tiles; 5 issues the MMAs (one thread) and owns TMEM;
-// 6-13 drain the accumulators, two warps per TMEM lane quarter on alternate
-// 16-column groups.  For BN <= 128 two TMEM accumulator pairs overlap one
+// 6-21 drain the accumulators, four warps per TMEM lane quarter taking its
+// 16-column groups in turn (the epilogue of a wide tile is not overlapped with
+// MMAs, so the more warps drain it the sooner TMEM is free: sixteen warps beat
+// eight by 2-3 % on the wide tiles).  For BN <= 128 two TMEM accumulator pairs overlap one
 // tile's epilogue with the next tile's MMAs (BN = 256 fills TMEM with one pair).
 #include "internal.h"
 #include "ptx.cuh"
@@ -65,9 +67,9 @@ constexpr int kTokWarp0 = 1;            // warps 1-4: token / activation loads
 constexpr int kTokThreads = 128;
 constexpr int kMmaWarp = 5;
 constexpr int kEpiWarp0 = 6;            // warps 6.. : the epilogue
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 constexpr int kGemmThreads = 32 * (kEpiWarp0 + kEpiWarps);
-constexpr int kWideEpiCols = 32;        // epilogue column group of tiles of 64 tokens or more
+constexpr int kWideEpiCols = 16;        // epilogue column group of tiles of 64 tokens or more
 constexpr int kRing = 4;                // claimed tile ids in flight
 constexpr unsigned long long kDrainNs = 20000000ull;
 
@@ -84,8 +86,8 @@ struct Layout {
   static constexpr int kT = Rings<BN>::kT;
   static constexpr int kTokBytes = BN * 128;
   static constexpr int kTOff = kW * kABytes;
-  // wide tiles stage each epilogue warp's 32-row x 32-token block in shared
-  // memory and store whole 16-byte pieces of token rows (2 KB per warp)
+  // wide tiles stage each epilogue warp's 32-row x 16-token block in shared
+  // memory and store whole 16-byte pieces of token rows (1 KB per warp)
   static constexpr bool kStageEpi = BN >= 256;
   static constexpr int kEpiOff = kTOff + kT * kTokBytes;
   static constexpr int kBarOff = kEpiOff + (kStageEpi ? kEpiWarps * kWideEpiCols * 64 : 0);  // tokens x 32 rows each
@@ -545,10 +547,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       }
     }
   } else {
-    // ================= epilogue (warps 6..13 -> TMEM lane quarters 2,3,0,1, twice)
+    // ================= epilogue (warps 6..21 -> TMEM lane quarters 2,3,0,1, four times)
     const int q = warp & 3;
-    // column groups of kEpiCols (32 for wide tiles: one TMEM wait per 32 columns);
-    // the two warps of a lane quarter take alternate groups
+    // column groups of kEpiCols (16: one TMEM wait per 16 columns);
+    // the warps of a lane quarter take its groups in turn
     constexpr int kEpiCols = BN >= 64 ? kWideEpiCols : 16;
     constexpr int kEpiStep = kEpiCols * (kEpiWarps / 4);  // the lane quarter's warps take groups in turn
     const int c_first = kEpiCols * ((warp - kEpiWarp0) >> 2);
