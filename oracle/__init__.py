@@ -36,7 +36,10 @@ Readings where the pages are silent (each also listed in the design notes):
 * top-k order: descending key, equal keys go to the lower expert index;
 * no epsilon in the sigmoid renormalisation; route_scale does not touch the
   shared expert; the shared expert is ungated and has intermediate size I;
-* the order of slots inside an expert segment is ascending flat slot t*k + j.
+* the order of slots inside an expert segment is ascending flat slot t*k + j;
+* FP8 expert weights (the Hy3 case's W8A8 deployments, format unspecified):
+  OCP E4M3 codes with one fp32 scale per output row, max|row| / 448, rounded
+  to nearest-even and saturated at 448; the layer uses bf16(value * scale).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 against closed forms, hand-worked examples (``tests/golden/``), brute force on
@@ -64,4 +67,8 @@ from .moe import (  # noqa: F401
     combine,
     layer_forward,
     layer_rows,
+    e4m3_value,
+    e4m3_encode,
+    quantize_rows_e4m3,
+    dequantize_rows_e4m3,
 )

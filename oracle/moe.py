@@ -234,6 +234,63 @@ def combine(y_sorted, inv, topk_w, z=None) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# FP8 (E4M3) expert weights with one scale per output row
+# ---------------------------------------------------------------------------
+# The Hy3 case lists W8A8 among its quantised deployments and quantises inside
+# the FusedMoE chain; the pages fix neither the format nor the scaling.  The
+# reading here (weight-only): every expert matrix is stored as OCP FP8 E4M3
+# codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is
+# subnormal; S.1111.111 is NaN, so the largest finite magnitude is 448) with one
+# fp32 scale per output row, scale = max|row| / 448 (1 for an all-zero row);
+# the layer uses bf16_RNE(value(code) * scale) in place of each bf16 weight.
+
+
+def e4m3_value(code) -> np.ndarray:
+    """Real value of E4M3 codes (uint8), NaN for the two NaN codes."""
+    c = np.asarray(code, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Nearest E4M3 code (ties to the even code), magnitudes past 448 saturated
+    to 448, NaN to the NaN code.  v is taken as float64 (the callers pass fp32
+    values)."""
+    v = np.asarray(v, dtype=np.float64)
+    pos = e4m3_value(np.arange(0x7F))          # 0 .. 448, increasing, codes 0x00..0x7E
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.clip(np.searchsorted(pos, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = a - pos[lo], pos[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.int64)
+    code = np.where(np.signbit(v), code | 0x80, code)
+    code = np.where(np.isnan(v), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def quantize_rows_e4m3(w):
+    """Per output row (last axis = input features): scale = fp32(max|w|) / 448 in
+    fp32 (1 if the row is zero), code = e4m3_encode(fp32(w) / scale) with the
+    division in fp32.  Returns (codes uint8, scales float32)."""
+    w32 = widen_bf16(w).astype(np.float32)
+    amax = np.abs(w32).max(axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    q = e4m3_encode((w32 / scale[..., None]).astype(np.float32))
+    return q, scale
+
+
+def dequantize_rows_e4m3(q, scale) -> np.ndarray:
+    """The bf16 weight a stored row stands for: bf16_RNE(fp32(value(code) * scale))."""
+    v = e4m3_value(q).astype(np.float32) * np.asarray(scale, dtype=np.float32)[..., None]
+    return bf16_round(v.astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
 # whole layer
 # ---------------------------------------------------------------------------
 

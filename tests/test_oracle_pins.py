@@ -347,3 +347,86 @@ def test_model_facts_match_workloads(golden_dir):
     assert (img.H, img.E, img.I, img.renorm_eps, img.score_mode) == (
         hi["hidden_size"], hi["routed_experts"], hi["expert_intermediate"], hi["clamp_min"], hi["score"])
     assert facts["router_split"]["scale"] == 1.0 / 256.0
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) expert weights
+# The format is the OCP 8-bit floating point specification's E4M3: its table of
+# special values gives the constants below (max normal S.1111.110 = 448, min
+# normal S.0001.000 = 2^-6, max subnormal S.0000.111 = 0.875 * 2^-6, min
+# subnormal S.0000.001 = 2^-9, S.1111.111 = NaN, no infinities).
+
+def test_e4m3_special_values():
+    v = oracle.e4m3_value(np.arange(256))
+    exact = {0x00: Fraction(0), 0x01: Fraction(1, 2 ** 9), 0x07: Fraction(7, 8) / 2 ** 6, 0x08: Fraction(1, 2 ** 6),
+             0x38: Fraction(1), 0x7E: Fraction(448), 0xB8: Fraction(-1), 0xFE: Fraction(-448)}
+    for c, x in exact.items():
+        assert Fraction(float(v[c])) == x, hex(c)
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.isnan(v).sum() == 2
+    assert v[0x80] == 0.0 and np.signbit(v[0x80])
+    pos = v[:0x7F]
+    assert (np.diff(pos) > 0).all()                      # codes 0x00..0x7E increase
+    assert np.array_equal(v[0x80:0xFF], -pos)             # sign-magnitude
+    # spacing: 2^-9 below 2^-5, then doubling at every binade (3 mantissa bits)
+    gaps = np.diff(pos)                                   # gaps[c] = value(c + 1) - value(c)
+    assert np.all(gaps[:8] == 2.0 ** -9)                 # subnormals and into the first binade
+    for e in range(1, 16):                                # codes 8e .. 8e + 7 span binade e
+        assert np.all(gaps[8 * e:8 * e + 8] == 2.0 ** (e - 10)), e
+
+
+def _encode_brute(x):
+    """Nearest of the 127 non-negative finite values by exhaustive search; a tie
+    goes to the even code; past 448 the magnitude is clamped to 448."""
+    pos = oracle.e4m3_value(np.arange(0x7F))
+    if np.isnan(x):
+        return 0x7F
+    a = min(abs(x), 448.0)
+    d = np.abs(pos - a)
+    best = np.flatnonzero(d == d.min())
+    c = int(best[0]) if len(best) == 1 else int(next(b for b in best if b % 2 == 0))
+    return c | (0x80 if math.copysign(1.0, x) < 0 else 0)
+
+
+def test_e4m3_encode_brute_force_ties_and_saturation():
+    pos = oracle.e4m3_value(np.arange(0x7F))
+    mids = (pos[:-1] + pos[1:]) / 2                        # exact ties between neighbours
+    rng = np.random.default_rng(5)
+    rand = np.concatenate([rng.standard_normal(2000) * s for s in (1e-3, 0.05, 1.0, 30.0, 300.0)])
+    vals = np.concatenate([pos, -pos, mids, -mids, rand, [500.0, -1e9, 448.0 + 15.9, 0.0, -0.0, np.nan]])
+    got = oracle.e4m3_encode(vals)
+    want = np.array([_encode_brute(float(x)) for x in vals], dtype=np.uint8)
+    assert np.array_equal(got, want)
+    # every finite code survives decode -> encode
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_value(codes)), codes.astype(np.uint8))
+
+
+def test_quantize_rows_bounds_and_zero_rows():
+    rng = np.random.default_rng(9)
+    w = W.normal_bf16(3, 7, (6, 256), 0.02)
+    w[2] = 0                                             # an all-zero row: scale 1, codes 0
+    q, s = oracle.quantize_rows_e4m3(w)
+    wf = W.bf16_to_f64(w)
+    assert s[2] == 1.0 and not q[2].any()
+    for r in (0, 1, 3, 4, 5):
+        assert s[r] == np.float32(np.float32(np.abs(wf[r]).max()) / np.float32(448.0))
+        assert int((q[r] & 0x7F).max()) == 0x7E           # the row maximum lands on 448
+    deq = oracle.dequantize_rows_e4m3(q, s)
+    # E4M3 keeps 3 fraction bits: relative error <= 2^-4 on normals, absolute
+    # <= 2^-10 * scale on subnormals, then one bf16 rounding (2^-9 relative)
+    err = np.abs(deq - wf)
+    bound = np.maximum(np.abs(wf) * (2.0 ** -4 + 2.0 ** -8), s[:, None].astype(np.float64) * 2.0 ** -10 * 1.01)
+    assert (err <= bound).all()
+
+
+def test_fp8_weights_on_the_grid_reduce_to_the_bf16_layer():
+    """Rows whose entries are E4M3 values times 2^-12 with the row maximum 448 *
+    2^-12 quantise with scale 2^-12 and dequantise back exactly, so the layer on
+    the dequantised weights is the bf16 layer bit for bit."""
+    rng = np.random.default_rng(4)
+    codes = rng.integers(0, 0x7F, size=(2, 16, 64)).astype(np.uint8)
+    codes[..., 0] = 0x7E
+    codes = codes | (rng.integers(0, 2, size=codes.shape).astype(np.uint8) << 7)
+    w = oracle.e4m3_value(codes) * 2.0 ** -12
+    q, s = oracle.quantize_rows_e4m3(w.astype(np.float32))
+    assert np.all(s == np.float32(2.0 ** -12))
+    assert np.array_equal(oracle.dequantize_rows_e4m3(q, s), w)
