@@ -39,7 +39,7 @@ Readings where the pages are silent (each also listed in the design notes):
 * the order of slots inside an expert segment is ascending flat slot t*k + j;
 * FP8 expert weights (the Hy3 case's W8A8 deployments, format unspecified):
   OCP E4M3 codes with one fp32 scale per output row, max|row| / 448, rounded
-  to nearest-even and saturated at 448; the layer uses bf16(value * scale).
+  to nearest-even and saturated at 448; the layer uses value * scale.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 against closed forms, hand-worked examples (``tests/golden/``), brute force on

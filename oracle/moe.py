@@ -242,7 +242,9 @@ def combine(y_sorted, inv, topk_w, z=None) -> np.ndarray:
 # codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is
 # subnormal; S.1111.111 is NaN, so the largest finite magnitude is 448) with one
 # fp32 scale per output row, scale = max|row| / 448 (1 for an all-zero row);
-# the layer uses bf16_RNE(value(code) * scale) in place of each bf16 weight.
+# the layer uses value(code) * scale, exactly, in place of each bf16 weight
+# (the scale multiplies the matrix product of a row, so no rounding of the
+# product of code and scale enters).
 
 
 def e4m3_value(code) -> np.ndarray:
@@ -285,9 +287,9 @@ def quantize_rows_e4m3(w):
 
 
 def dequantize_rows_e4m3(q, scale) -> np.ndarray:
-    """The bf16 weight a stored row stands for: bf16_RNE(fp32(value(code) * scale))."""
-    v = e4m3_value(q).astype(np.float32) * np.asarray(scale, dtype=np.float32)[..., None]
-    return bf16_round(v.astype(np.float32))
+    """The weight a stored row stands for: value(code) * scale, exact in float64
+    (at most 4 significant bits times 24)."""
+    return e4m3_value(q) * np.asarray(scale, dtype=np.float64)[..., None]
 
 
 # ---------------------------------------------------------------------------
