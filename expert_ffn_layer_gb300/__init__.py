@@ -9,6 +9,8 @@ Function names follow the C ABI:
     moe_route, moe_permute, moe_expert_ffn (= moe_expert_gate_up + moe_expert_down),
     moe_combine, moe_layer_forward,
     moe_fused_moe (routing given, stacked [E, 2I, H] gate/up weights),
+    moe_quantize_fp8_rows, moe_expert_ffn_fp8, moe_layer_forward_fp8 (FP8 E4M3
+    expert weights, one scale per row; see Fp8Experts / quantize_fp8_experts),
     moe_workspace_bytes, moe_ws_init, moe_ws_read_error, moe_check_dims
 
 Tensors are torch tensors on the current CUDA device: bf16 activations and
@@ -32,7 +34,8 @@ SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
 
 EXPORTS = ("moe_status_string", "moe_check_dims", "moe_workspace_bytes", "moe_ws_init", "moe_ws_read_error",
            "moe_route", "moe_permute", "moe_expert_ffn", "moe_expert_gate_up", "moe_expert_down", "moe_combine",
-           "moe_layer_forward", "moe_fused_moe", "moe_expert_ffn_noalloc", "moe_selftest_wait_timeout")
+           "moe_layer_forward", "moe_fused_moe", "moe_expert_ffn_noalloc", "moe_selftest_wait_timeout",
+           "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_layer_forward_fp8")
 
 
 class MoeError(RuntimeError):
@@ -48,6 +51,12 @@ class MoeDims(ctypes.Structure):
 
     def __repr__(self):
         return "MoeDims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+class MoeFp8Experts(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("gate", "up", "down", "gate_scale", "up_scale", "down_scale",
+                                                "s_gate", "s_up", "s_down", "s_gate_scale", "s_up_scale",
+                                                "s_down_scale")]
 
 
 _lib = None
@@ -83,6 +92,9 @@ def load() -> ctypes.CDLL:
         "moe_combine": (st, [D, P, P, P, P, P, P]),
         "moe_layer_forward": (st, [D, P, P, P, P, P, P, P, P, P, P, P, C, P]),
         "moe_fused_moe": (st, [D, P, P, P, P, P, P, P, P, P, C, P]),
+        "moe_quantize_fp8_rows": (st, [P, ctypes.c_int64, ctypes.c_int, P, P, P]),
+        "moe_expert_ffn_fp8": (st, [D, P, P, P, ctypes.POINTER(MoeFp8Experts), P, P, P, C, P]),
+        "moe_layer_forward_fp8": (st, [D, P, P, P, ctypes.POINTER(MoeFp8Experts), P, P, C, P]),
         "moe_selftest_wait_timeout": (st, [P, C, ctypes.c_ulonglong, P]),
     }
     for name, (res, args) in sig.items():
@@ -280,6 +292,73 @@ def fused_moe(hidden, topk_index, topk_weight, w_gate_up, w_down, output=None, w
     moe_fused_moe(d, hidden, topk_index, topk_weight, w_gate_up, w_down, ws_gate_up, ws_down, output, workspace,
                   stream)
     return output
+
+
+def moe_quantize_fp8_rows(src, codes, scales, stream=None) -> None:
+    """codes [R, C] uint8 (E4M3) and scales [R] fp32 of a bf16 matrix [R, C] (any
+    leading dims are rows)."""
+    C = src.shape[-1]
+    R = src.numel() // C if C else 0
+    _check(src, torch.bfloat16, src.shape, "src")
+    _check(codes, torch.uint8, src.shape, "codes")
+    _check(scales, torch.float32, src.shape[:-1], "scales")
+    _call("moe_quantize_fp8_rows", _ptr(src), R, C, _ptr(codes), _ptr(scales), _stream(stream))
+
+
+class Fp8Experts:
+    """Device tensors of FP8 expert weights (E4M3 codes + one fp32 scale per
+    row) and the C struct that points at them."""
+
+    NAMES = ("gate", "up", "down", "s_gate", "s_up", "s_down")
+
+    def __init__(self, **tensors):
+        self.t = tensors  # name -> (codes uint8, scales fp32) or None
+        st = MoeFp8Experts()
+        for n in self.NAMES:
+            pair = tensors.get(n)
+            setattr(st, n, pair[0].data_ptr() if pair is not None else None)
+            setattr(st, n + "_scale", pair[1].data_ptr() if pair is not None else None)
+        self.struct = st
+
+
+def quantize_fp8_experts(w_gate, w_up, w_down, ws_gate=None, ws_up=None, ws_down=None, stream=None) -> Fp8Experts:
+    """Quantise bf16 expert weights (and the shared expert's, if given) with
+    moe_quantize_fp8_rows on the device."""
+    out = {}
+    for n, w in (("gate", w_gate), ("up", w_up), ("down", w_down), ("s_gate", ws_gate), ("s_up", ws_up),
+                 ("s_down", ws_down)):
+        if w is None:
+            continue
+        codes = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+        scales = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+        moe_quantize_fp8_rows(w, codes, scales, stream)
+        out[n] = (codes, scales)
+    return Fp8Experts(**out)
+
+
+def moe_expert_ffn_fp8(d: MoeDims, hidden, perm, offsets, w: Fp8Experts, y_sorted, y_shared, ws, stream=None) -> None:
+    S = d.T * d.top_k
+    _check(hidden, torch.bfloat16, (d.T, d.H), "hidden")
+    _check(perm, torch.int32, (S,), "perm")
+    _check(offsets, torch.int32, (d.E + 1,), "offsets")
+    _check(y_sorted, torch.bfloat16, (S, d.H), "y_sorted")
+    _check(w.t["gate"][0], torch.uint8, (d.E, d.I, d.H), "gate codes")
+    _check(w.t["down"][0], torch.uint8, (d.E, d.H, d.I), "down codes")
+    if d.has_shared:
+        _check(y_shared, torch.bfloat16, (d.T, d.H), "y_shared")
+        _check(w.t["s_gate"][0], torch.uint8, (d.I_shared, d.H), "shared gate codes")
+    _call("moe_expert_ffn_fp8", ctypes.byref(d), _ptr(hidden), _ptr(perm), _ptr(offsets), ctypes.byref(w.struct),
+          _ptr(y_sorted), _ptr(y_shared), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def moe_layer_forward_fp8(d: MoeDims, hidden, router_w, expert_bias, w: Fp8Experts, out, ws, stream=None) -> None:
+    _check(hidden, torch.bfloat16, (d.T, d.H), "hidden")
+    _check(router_w, torch.float32, (d.E, d.H), "router_w")
+    _check(expert_bias, torch.float32, (d.E,), "expert_bias")
+    _check(out, torch.bfloat16, (d.T, d.H), "out")
+    _check(w.t["gate"][0], torch.uint8, (d.E, d.I, d.H), "gate codes")
+    _call("moe_layer_forward_fp8", ctypes.byref(d), _ptr(hidden), _ptr(router_w), _ptr(expert_bias),
+          ctypes.byref(w.struct), _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
 
 
 def moe_selftest_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> None:

@@ -15,7 +15,7 @@ CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libmoe_gb300.so"
 INCLUDE = PKG.parent / "include"
-SOURCES = ["api.cu", "router.cu", "permute.cu", "expert_gemm.cu", "combine.cu", "selftest.cu"]
+SOURCES = ["api.cu", "router.cu", "permute.cu", "expert_gemm.cu", "combine.cu", "selftest.cu", "fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", str(INCLUDE)]

@@ -76,6 +76,20 @@ bool map_bf16_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, 
   const uint32_t box[2] = {64, box_rows};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
+// E4M3 codes [rows][cols] (uint8), box {64 codes, box_rows}, no swizzle
+bool map_u8_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t str[1] = {cols};
+  const uint32_t box[2] = {64, box_rows};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+// stacked E4M3 codes [n][rows][cols], box {64, box_rows, 1}, no swizzle
+bool map_u8_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t n, uint32_t box_rows) {
+  const uint64_t dims[3] = {cols, rows, n};
+  const uint64_t str[2] = {cols, cols * rows};
+  const uint32_t box[3] = {64, box_rows, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
 // stacked bf16 [n][rows][cols] (consecutive matrices `stride_rows` rows apart,
 // rows by default), box {64, box_rows, 1}, 128-byte swizzle
 bool map_bf16_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t n, uint32_t box_rows,
@@ -219,7 +233,8 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
                             const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
                             const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
                             const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws,
-                            cudaStream_t stream, bool pdl, uint64_t gu_stride = 0) {
+                            cudaStream_t stream, bool pdl, uint64_t gu_stride = 0,
+                            const moe_fp8_experts *q = nullptr) {
   const WsLayout L = ws_layout(d);
   GemmParams g;
   std::memset(&g, 0, sizeof(g));
@@ -242,6 +257,25 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
   g.y = reinterpret_cast<__nv_bfloat16 *>(y_sorted);
   g.y_s = reinterpret_cast<__nv_bfloat16 *>(y_shared);
   bool ok = true;
+  if (q != nullptr) {  // FP8 expert weights: maps of the codes, and the row scales
+    g.q8 = 1;
+    g.sc_g = q->gate_scale;
+    g.sc_u = q->up_scale;
+    g.sc_d = q->down_scale;
+    g.sc_sg = q->s_gate_scale;
+    g.sc_su = q->s_up_scale;
+    g.sc_sd = q->s_down_scale;
+    ok = map_u8_3d(&g.map_wg, q->gate, d.H, d.I, d.E, 128) && map_u8_3d(&g.map_wu, q->up, d.H, d.I, d.E, 128) &&
+         map_u8_3d(&g.map_wd, q->down, d.I, d.H, d.E, 128);
+    if (d.has_shared)
+      ok = ok && map_u8_2d(&g.map_sg, q->s_gate, d.H, g.Is, 128) && map_u8_2d(&g.map_su, q->s_up, d.H, g.Is, 128) &&
+           map_u8_2d(&g.map_sd, q->s_down, g.Is, d.H, 128);
+    for (int b = 0; b < 4; ++b) ok = ok && map_bf16_2d(&g.map_act[b], g.act, d.I, g.S, 16u << b);
+    if (d.has_shared)
+      for (int b = 0; b < 4; ++b) ok = ok && map_bf16_2d(&g.map_acts[b], g.act_s, g.Is, d.T, 16u << b);
+    if (!ok) return MOE_ERR_CUDA;
+    return cuda_status(launch_expert_ffn(g, gemm_tile_n(d.T, d.top_k, d.E), num_sms(), stream, pdl));
+  }
   if (phases & 1) {
     ok = ok && map_bf16_3d(&g.map_wg, w_gate, d.H, d.I, d.E, 128, gu_stride) &&
          map_bf16_3d(&g.map_wu, w_up, d.H, d.I, d.E, 128, gu_stride);
@@ -300,6 +334,16 @@ moe_status do_combine(const moe_dims &d, const moe_bf16 *y_sorted, const moe_bf1
 }
 
 bool ptr_ok(const void *p) { return p != nullptr && aligned16(p); }
+
+bool fp8_ok(const moe_dims &d, const moe_fp8_experts *q) {
+  if (q == nullptr || !ptr_ok(q->gate) || !ptr_ok(q->up) || !ptr_ok(q->down) || !ptr_ok(q->gate_scale) ||
+      !ptr_ok(q->up_scale) || !ptr_ok(q->down_scale))
+    return false;
+  if (d.has_shared && (!ptr_ok(q->s_gate) || !ptr_ok(q->s_up) || !ptr_ok(q->s_down) || !ptr_ok(q->s_gate_scale) ||
+                       !ptr_ok(q->s_up_scale) || !ptr_ok(q->s_down_scale)))
+    return false;
+  return true;
+}
 
 // Steps a3-a9 from a given routing, with the gate and up projections of every
 // expert stacked in one tensor: permutation, grouped expert FFN, combine.
@@ -479,6 +523,53 @@ MOE_API moe_status moe_fused_moe(const moe_dims *d, const moe_bf16 *hidden, cons
   if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
   return do_fused_moe(*d, hidden, topk_idx, topk_w, w_gate_up, w_down, ws_gate_up, ws_down, out, ws,
                       (cudaStream_t)stream);
+}
+
+MOE_API moe_status moe_quantize_fp8_rows(const moe_bf16 *src, int64_t rows, int cols, uint8_t *codes, float *scales,
+                                         void *stream) {
+  if (rows < 0 || cols <= 0 || cols % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!ptr_ok(src) || !ptr_ok(codes) || scales == nullptr || ((uintptr_t)scales & 3u) != 0) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_rows(reinterpret_cast<const __nv_bfloat16 *>(src), codes, scales, (long long)rows,
+                                          cols, (cudaStream_t)stream));
+}
+
+MOE_API moe_status moe_expert_ffn_fp8(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
+                                      const int32_t *offsets, const moe_fp8_experts *w, moe_bf16 *y_sorted,
+                                      moe_bf16 *y_shared, void *ws, size_t ws_bytes, void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(hidden) || !ptr_ok(perm) || !ptr_ok(offsets) || !ptr_ok(y_sorted) || !fp8_ok(*d, w))
+    return MOE_ERR_INVALID_ARG;
+  if (d->has_shared && !ptr_ok(y_shared)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  return do_expert_phases(*d, 3, hidden, perm, offsets, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                          y_sorted, y_shared, ws, (cudaStream_t)stream, true, 0, w);
+}
+
+MOE_API moe_status moe_layer_forward_fp8(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
+                                         const float *expert_bias, const moe_fp8_experts *w, moe_bf16 *out, void *ws,
+                                         size_t ws_bytes, void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(hidden) || !ptr_ok(router_w) || !ptr_ok(out) || !fp8_ok(*d, w)) return MOE_ERR_INVALID_ARG;
+  if (expert_bias != nullptr && !aligned16(expert_bias)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  const WsLayout L = ws_layout(*d);
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t *idx = at<int32_t>(ws, L.topk_idx);
+  float *wt = at<float>(ws, L.topk_w);
+  int32_t *perm = at<int32_t>(ws, L.perm), *inv = at<int32_t>(ws, L.inv);
+  int32_t *offs = at<int32_t>(ws, L.offsets);
+  moe_bf16 *y = at<moe_bf16>(ws, L.y_sorted), *z = at<moe_bf16>(ws, L.y_shared);
+  if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, wt, ws, s, true)) != MOE_OK) return st;
+  if ((st = do_permute(*d, idx, at<int32_t>(ws, L.counts), offs, perm, inv, ws, s, true)) != MOE_OK) return st;
+  if ((st = do_expert_phases(*d, 3, hidden, perm, offs, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, y, z,
+                             ws, s, true, 0, w)) != MOE_OK)
+    return st;
+  return do_combine(*d, y, z, inv, wt, out, s, true);
 }
 
 MOE_API moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,

@@ -53,6 +53,8 @@
 // MMAs, so the more warps drain it the sooner TMEM is free: sixteen warps beat
 // eight by 2-3 % on the wide tiles).  For BN <= 128 two TMEM accumulator pairs overlap one
 // tile's epilogue with the next tile's MMAs (BN = 256 fills TMEM with one pair).
+#include <cuda_fp8.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -71,29 +73,40 @@ constexpr int kEpiWarps = 16;
 constexpr int kGemmThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kWideEpiCols = 16;        // epilogue column group of tiles of 64 tokens or more
 constexpr int kRing = 4;                // claimed tile ids in flight
+// FP8 weights: TMA brings the E4M3 codes of a K step (two 128-row x 64-code
+// boxes, 16 KB) into a ring of their own; eight converter warps (taking the
+// place of eight epilogue warps) write them as bf16 into the weight slots
+constexpr int kQBytes = 2 * 128 * 64;
+constexpr int kCvtWarps = 8;
 constexpr unsigned long long kDrainNs = 20000000ull;
 
-// Ring depths: weight slots of 32 KB and token slots of BN x 128 bytes.
-template <int BN>
+// Ring depths: weight slots of 32 KB and token slots of BN x 128 bytes; with
+// FP8 weights, code slots of 16 KB (the bytes in flight from HBM) and three
+// bf16 weight slots between the converters and the MMAs.
+template <int BN, bool Q8>
 struct Rings {
-  static constexpr int kW = BN >= 256 ? 3 : BN >= 240 ? 4 : BN >= 128 ? 5 : 6;
+  static constexpr int kW = Q8 ? 3 : BN >= 256 ? 3 : BN >= 240 ? 4 : BN >= 128 ? 5 : 6;
+  static constexpr int kQ = Q8 ? (BN >= 128 ? 4 : 6) : 0;
   static constexpr int kT = BN >= 64 ? 3 : 4;
 };
 
-template <int BN>
+template <int BN, bool Q8>
 struct Layout {
-  static constexpr int kW = Rings<BN>::kW;
-  static constexpr int kT = Rings<BN>::kT;
+  static constexpr int kW = Rings<BN, Q8>::kW;
+  static constexpr int kQ = Rings<BN, Q8>::kQ;
+  static constexpr int kT = Rings<BN, Q8>::kT;
+  static constexpr int kEpiW = Q8 ? kEpiWarps - kCvtWarps : kEpiWarps;  // epilogue warps
   static constexpr int kTokBytes = BN * 128;
-  static constexpr int kTOff = kW * kABytes;
+  static constexpr int kQOff = kW * kABytes;
+  static constexpr int kTOff = kQOff + kQ * kQBytes;
   // wide tiles stage each epilogue warp's 32-row x 16-token block in shared
   // memory and store whole 16-byte pieces of token rows (1 KB per warp)
   static constexpr bool kStageEpi = BN >= 256;
   static constexpr int kEpiOff = kTOff + kT * kTokBytes;
-  static constexpr int kBarOff = kEpiOff + (kStageEpi ? kEpiWarps * kWideEpiCols * 64 : 0);  // tokens x 32 rows each
+  static constexpr int kBarOff = kEpiOff + (kStageEpi ? kEpiW * kWideEpiCols * 64 : 0);  // tokens x 32 rows each
   // wfull, wempty per weight slot; tfull, tempty per token slot; acc full[2],
-  // acc empty[2]; drain; id_full[kRing], id_empty[kRing]
-  static constexpr int kNumBars = 2 * kW + 2 * kT + 5 + 2 * kRing;
+  // acc empty[2]; drain; id_full[kRing], id_empty[kRing]; qfull, qempty per code slot
+  static constexpr int kNumBars = 2 * kW + 2 * kT + 5 + 2 * kRing + 2 * kQ;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;     // tmem slot, abort flag, ring of tile ids
   static constexpr int kStart1Off = kMiscOff + 64;
   static constexpr int kStart2Off = kStart1Off + 4 * kMaxSeg;
@@ -108,7 +121,8 @@ struct Layout {
                                         : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kTmemUsed <= 512, "TMEM budget");
-  static_assert(kW <= 16 && kT <= 16, "issue masks");
+  static_assert(kW <= 16 && kT <= 16 && kQ <= 16, "issue masks");
+  static_assert(!Q8 || BN <= 128, "FP8 weights run the narrow tiles");
 };
 
 struct Tile {
@@ -216,12 +230,28 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return g * u * r;
 }
 
+// Eight E4M3 codes (two little-endian words, first code in the low byte) to the
+// eight bf16 values they encode, exactly (every E4M3 value is a bf16 value; the
+// row scale is applied to the fp32 accumulators in the epilogue instead).
+__device__ __forceinline__ uint4 e4m3x8_to_bf16(uint32_t w0, uint32_t w1) {
+  const uint32_t pr[4] = {w0 & 0xFFFFu, w0 >> 16, w1 & 0xFFFFu, w1 >> 16};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)pr[j], __NV_E4M3);
+    const float2 f = __half22float2(__half2(hr));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    o[j] = *reinterpret_cast<const uint32_t *>(&b);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 }  // namespace
 
-template <int BN>
+template <int BN, bool Q8>
 __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __grid_constant__ GemmParams p) {
-  using L = Layout<BN>;
-  constexpr int KW = L::kW, KT = L::kT;
+  using L = Layout<BN, Q8>;
+  constexpr int KW = L::kW, KT = L::kT, KQ = L::kQ, EW = L::kEpiW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = (uint64_t *)(smem + L::kBarOff);
@@ -242,13 +272,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   const uint32_t drain_bar = smem_u32(&bars[2 * KW + 2 * KT + 4]);
   auto id_full = [&](int r) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + r]); };
   auto id_empty = [&](int r) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + kRing + r]); };
+  auto qfull_bar = [&](int s) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + 2 * kRing + s]); };
+  auto qempty_bar = [&](int s) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + 2 * kRing + KQ + s]); };
+  auto q_smem = [&](int s) { return smem_u32(smem + L::kQOff + s * kQBytes); };
   auto w_smem = [&](int s) { return smem_u32(smem + s * kABytes); };
   auto t_smem = [&](int s) { return smem_u32(smem + L::kTOff + s * L::kTokBytes); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < KW; ++s) {
-      mbar_init(wfull_bar(s), 1);   // the weight loader's expect_tx arrival
-      mbar_init(wempty_bar(s), 1);  // MMA commit
+      mbar_init(wfull_bar(s), Q8 ? kCvtWarps : 1);  // the weight loader's expect_tx arrival, or the converters
+      mbar_init(wempty_bar(s), 1);                  // MMA commit
+    }
+    for (int s = 0; s < KQ; ++s) {
+      mbar_init(qfull_bar(s), 1);           // the loader's expect_tx arrival
+      mbar_init(qempty_bar(s), kCvtWarps);  // converters done reading
     }
     for (int s = 0; s < KT; ++s) {
       mbar_init(tfull_bar(s), kTokThreads);  // one arrival per loader thread (cp.async, or the TMA expect_tx)
@@ -256,12 +293,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(afull_bar(a), 1);
-      mbar_init(aempty_bar(a), kEpiWarps);
+      mbar_init(aempty_bar(a), EW);
     }
     mbar_init(drain_bar, 1);
     for (int r = 0; r < kRing; ++r) {
       mbar_init(id_full(r), 1);
-      mbar_init(id_empty(r), 1 + 4 + kEpiWarps);  // MMA thread + 4 token-loader warps + epilogue warps
+      mbar_init(id_empty(r), 1 + 4 + EW + (Q8 ? kCvtWarps : 0));  // MMA, token loaders, epilogue, converters
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -329,8 +366,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   bool ok = true;
 
   if (warp == kWWarp) {
-    // ================= tile claims and weight loads (one thread)
+    // ================= tile claims and weight loads (one thread); FP8 weights
+    // go to the code slots, bf16 weights straight to the weight slots
     if (lane == 0) {
+      constexpr int NS = Q8 ? KQ : KW;
       const uint64_t pol_w = policy_evict_first();
       int ws = 0;
       uint32_t wph = 0;
@@ -347,39 +386,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
         const int i0 = tl.rb * (tl.phase == 0 ? 128 : 256);
         for (int kb = 0; kb < tl.nk; ++kb) {
-          ok = mbar_wait(wempty_bar(ws), wph ^ 1u, err, abort_flag);
+          const uint32_t fb = Q8 ? qfull_bar(ws) : wfull_bar(ws);
+          ok = mbar_wait(Q8 ? qempty_bar(ws) : wempty_bar(ws), wph ^ 1u, err, abort_flag);
           if (!ok) break;
           const int k0 = kb * 64;
-          mbar_arrive_expect_tx(wfull_bar(ws), (uint32_t)kABytes);
+          mbar_arrive_expect_tx(fb, (uint32_t)(Q8 ? kQBytes : kABytes));
           issued |= 1u << ws;
           issued_par = (issued_par & ~(1u << ws)) | (wph << ws);
-          const uint32_t a0 = w_smem(ws), a1 = a0 + 16384;
+          const uint32_t a0 = Q8 ? q_smem(ws) : w_smem(ws), a1 = a0 + (Q8 ? kQBytes / 2 : kABytes / 2);
           if (tl.phase == 0) {
             if (tl.shared) {
-              tma_load_2d_hint(a0, &p.map_sg, wfull_bar(ws), k0, i0, pol_w);
-              tma_load_2d_hint(a1, &p.map_su, wfull_bar(ws), k0, i0, pol_w);
+              tma_load_2d_hint(a0, &p.map_sg, fb, k0, i0, pol_w);
+              tma_load_2d_hint(a1, &p.map_su, fb, k0, i0, pol_w);
             } else {
-              tma_load_3d_hint(a0, &p.map_wg, wfull_bar(ws), k0, i0, tl.seg, pol_w);
-              tma_load_3d_hint(a1, &p.map_wu, wfull_bar(ws), k0, i0, tl.seg, pol_w);
+              tma_load_3d_hint(a0, &p.map_wg, fb, k0, i0, tl.seg, pol_w);
+              tma_load_3d_hint(a1, &p.map_wu, fb, k0, i0, tl.seg, pol_w);
             }
           } else {
             if (tl.shared) {
-              tma_load_2d_hint(a0, &p.map_sd, wfull_bar(ws), k0, i0, pol_w);
-              tma_load_2d_hint(a1, &p.map_sd, wfull_bar(ws), k0, i0 + 128, pol_w);
+              tma_load_2d_hint(a0, &p.map_sd, fb, k0, i0, pol_w);
+              tma_load_2d_hint(a1, &p.map_sd, fb, k0, i0 + 128, pol_w);
             } else {
-              tma_load_3d_hint(a0, &p.map_wd, wfull_bar(ws), k0, i0, tl.seg, pol_w);
-              tma_load_3d_hint(a1, &p.map_wd, wfull_bar(ws), k0, i0 + 128, tl.seg, pol_w);
+              tma_load_3d_hint(a0, &p.map_wd, fb, k0, i0, tl.seg, pol_w);
+              tma_load_3d_hint(a1, &p.map_wd, fb, k0, i0 + 128, tl.seg, pol_w);
             }
           }
-          if (++ws == KW) {
+          if (++ws == NS) {
             ws = 0;
             wph ^= 1u;
           }
         }
       }
       if (!ok)
-        for (int s = 0; s < KW; ++s)
-          if ((issued >> s) & 1u) mbar_wait_drain(wfull_bar(s), (issued_par >> s) & 1u);
+        for (int s = 0; s < NS; ++s)
+          if ((issued >> s) & 1u) mbar_wait_drain(Q8 ? qfull_bar(s) : wfull_bar(s), (issued_par >> s) & 1u);
     }
   } else if (warp < kTokWarp0 + 4) {
     // ================= token rows (gate/up) or activation rows (down)
@@ -546,13 +586,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         mbar_wait_drain(drain_bar, 0);
       }
     }
-  } else {
-    // ================= epilogue (warps 6..21 -> TMEM lane quarters 2,3,0,1, four times)
+  } else if (warp < kEpiWarp0 + EW) {
+    // ================= epilogue (warps 6..21 -> TMEM lane quarters 2,3,0,1, four times;
+    // with FP8 weights warps 6..13, twice)
     const int q = warp & 3;
     // column groups of kEpiCols (16: one TMEM wait per 16 columns);
     // the warps of a lane quarter take its groups in turn
     constexpr int kEpiCols = BN >= 64 ? kWideEpiCols : 16;
-    constexpr int kEpiStep = kEpiCols * (kEpiWarps / 4);  // the lane quarter's warps take groups in turn
+    constexpr int kEpiStep = kEpiCols * (EW / 4);  // the lane quarter's warps take groups in turn
     const int c_first = kEpiCols * ((warp - kEpiWarp0) >> 2);
     __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(smem + L::kEpiOff + (warp - kEpiWarp0) * kEpiCols * 64);
     const int r = 32 * q + lane;  // weight row within the 128-row half
@@ -571,6 +612,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       if (!ok) break;
       tc_fence_after();
       const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * 2 * BN);
+      // FP8 weights: the accumulators hold sum(value(code) * x); this lane's
+      // row scales turn them into the products with the weights
+      float s0 = 1.0f, s1 = 1.0f;
+      if constexpr (Q8) {
+        if (tl.phase == 0) {
+          const int ii = tl.rb * 128 + r;
+          if (ii < (tl.shared ? p.Is : p.I)) {
+            s0 = __ldg((tl.shared ? p.sc_sg : p.sc_g + (size_t)tl.seg * p.I) + ii);
+            s1 = __ldg((tl.shared ? p.sc_su : p.sc_u + (size_t)tl.seg * p.I) + ii);
+          }
+        } else {
+          const int ha = tl.rb * 256 + r, hb = ha + 128;
+          const float *sp = tl.shared ? p.sc_sd : p.sc_d + (size_t)tl.seg * p.H;
+          if (ha < p.H) s0 = __ldg(sp + ha);
+          if (hb < p.H) s1 = __ldg(sp + hb);
+        }
+      }
       if constexpr (L::kStageEpi) {
         // lane j of the warp owns weight row first + j; a group of ncol tokens is
         // written to the staging block as [token][32 rows] bf16, then each lane
@@ -649,7 +707,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
 #pragma unroll
               for (int j = 0; j < 32; ++j)
                 if (c + j < tl.ntok)
-                  out[(size_t)(tl.row0 + c + j) * ld + ii] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
+                  out[(size_t)(tl.row0 + c + j) * ld + ii] =
+                      __float2bfloat16_rn(Q8 ? silu_mul(g[j] * s0, u[j] * s1) : silu_mul(g[j], u[j]));
             }
           } else {
             for (int c16 = c; c16 < min(c + kEpiCols, tl.N); c16 += 16) {
@@ -661,7 +720,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                   if (c16 + j < tl.ntok)
-                    out[(size_t)(tl.row0 + c16 + j) * ld + ii] = __float2bfloat16_rn(silu_mul(g[j], u[j]));
+                    out[(size_t)(tl.row0 + c16 + j) * ld + ii] =
+                        __float2bfloat16_rn(Q8 ? silu_mul(g[j] * s0, u[j] * s1) : silu_mul(g[j], u[j]));
               }
             }
           }
@@ -679,8 +739,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
             for (int j = 0; j < 32; ++j) {
               if (c + j < tl.ntok) {
                 __nv_bfloat16 *row = out + (size_t)(tl.row0 + c + j) * p.H;
-                if (ha < p.H) __stcs(row + ha, __float2bfloat16_rn(va[j]));
-                if (hb < p.H) __stcs(row + hb, __float2bfloat16_rn(vb[j]));
+                if (ha < p.H) __stcs(row + ha, __float2bfloat16_rn(Q8 ? va[j] * s0 : va[j]));
+                if (hb < p.H) __stcs(row + hb, __float2bfloat16_rn(Q8 ? vb[j] * s1 : vb[j]));
               }
             }
           } else {
@@ -693,8 +753,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
               for (int j = 0; j < 16; ++j) {
                 if (c16 + j < tl.ntok) {
                   __nv_bfloat16 *row = out + (size_t)(tl.row0 + c16 + j) * p.H;
-                  if (ha < p.H) __stcs(row + ha, __float2bfloat16_rn(va[j]));
-                  if (hb < p.H) __stcs(row + hb, __float2bfloat16_rn(vb[j]));
+                  if (ha < p.H) __stcs(row + ha, __float2bfloat16_rn(Q8 ? va[j] * s0 : va[j]));
+                  if (hb < p.H) __stcs(row + hb, __float2bfloat16_rn(Q8 ? vb[j] * s1 : vb[j]));
                 }
               }
             }
@@ -707,8 +767,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       if (tl.phase == 0 && (p.phases & 2)) {
         // publish: this gate/up tile's activations are written (release to the down tiles)
         __threadfence();
-        named_bar_sync(2, 32 * kEpiWarps);
+        named_bar_sync(2, 32 * EW);
         if (warp == kEpiWarp0 && lane == 0) atomicAdd(done1 + tl.seg, 1u);
+      }
+    }
+  } else if constexpr (Q8) {
+    // ================= FP8 weights (warps 14..21): codes -> bf16 weight slots
+    // (the values of the codes; the epilogue applies each row's scale).
+    // Converter warp cw takes rows 32 (cw & 3) .. + 31 of box cw >> 2; per
+    // pass, lane l converts 16 codes (chunk l & 3) of row 8 it + (l >> 2), so a
+    // warp reads 512 contiguous bytes and writes whole 128-byte swizzled rows.
+    const int cw = warp - (kEpiWarp0 + EW);
+    const int box = cw >> 2, c = lane & 3;
+    int ws = 0, qs = 0;
+    uint32_t wph = 0, qph = 0;
+    for (int i = 0; ok; ++i) {
+      const int rs = i % kRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(id_full(rs), (uint32_t)(i / kRing) & 1u, err, abort_flag));
+      if (!ok) break;
+      const int t = ring[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(id_empty(rs));
+      if (t < 0) break;
+      const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+      for (int kb = 0; kb < tl.nk; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(qfull_bar(qs), qph, err, abort_flag) &&
+                                         mbar_wait(wempty_bar(ws), wph ^ 1u, err, abort_flag));
+        if (!ok) break;
+        const uint8_t *src = smem + L::kQOff + qs * kQBytes + box * (kQBytes / 2);
+        uint8_t *dst = smem + ws * kABytes + box * (kABytes / 2);
+        uint4 v[4];  // every read first: the stores cannot then hold back the next loads
+#pragma unroll
+        for (int it = 0; it < 4; ++it)
+          v[it] = *reinterpret_cast<const uint4 *>(src + (32 * (cw & 3) + 8 * it + (lane >> 2)) * 64 + c * 16);
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int rr = 32 * (cw & 3) + 8 * it + (lane >> 2);
+          *reinterpret_cast<uint4 *>(dst + rr * 128 + (((2 * c) ^ (rr & 7)) << 4)) = e4m3x8_to_bf16(v[it].x, v[it].y);
+          *reinterpret_cast<uint4 *>(dst + rr * 128 + (((2 * c + 1) ^ (rr & 7)) << 4)) =
+              e4m3x8_to_bf16(v[it].z, v[it].w);
+        }
+        fence_proxy_async_smem();  // generic-proxy writes read by the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(wfull_bar(ws));
+          mbar_arrive(qempty_bar(qs));
+        }
+        if (++ws == KW) {
+          ws = 0;
+          wph ^= 1u;
+        }
+        if (++qs == KQ) {
+          qs = 0;
+          qph ^= 1u;
+        }
       }
     }
   }
@@ -746,32 +858,41 @@ int gemm_tile_n(int T, int top_k, int E) {
 }
 
 namespace {
-template <int BN>
+template <int BN, bool Q8>
 cudaError_t launch_one(const GemmParams &p, int num_ctas, cudaStream_t stream, bool pdl) {
-  using L = Layout<BN>;
+  using L = Layout<BN, Q8>;
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
     cudaError_t e =
-        cudaFuncSetAttribute(expert_ffn_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
+        cudaFuncSetAttribute(expert_ffn_kernel<BN, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
   void *args[] = {(void *)&p};
-  return launch_ex((const void *)expert_ffn_kernel<BN>, dim3(num_ctas), dim3(kGemmThreads), L::kSmem, stream, pdl, 1,
+  return launch_ex((const void *)expert_ffn_kernel<BN, Q8>, dim3(num_ctas), dim3(kGemmThreads), L::kSmem, stream, pdl, 1,
                    args);
 }
 }  // namespace
 
 cudaError_t launch_expert_ffn(const GemmParams &p, int bn, int num_ctas, cudaStream_t stream, bool pdl) {
+  if (p.q8) {  // FP8 weights: narrow tiles only (the code ring takes the shared memory of wide token slots)
+    switch (bn < 128 ? bn : 128) {
+      case 16: return launch_one<16, true>(p, num_ctas, stream, pdl);
+      case 32: return launch_one<32, true>(p, num_ctas, stream, pdl);
+      case 64: return launch_one<64, true>(p, num_ctas, stream, pdl);
+      case 128: return launch_one<128, true>(p, num_ctas, stream, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (bn) {
-    case 16: return launch_one<16>(p, num_ctas, stream, pdl);
-    case 32: return launch_one<32>(p, num_ctas, stream, pdl);
-    case 64: return launch_one<64>(p, num_ctas, stream, pdl);
-    case 128: return launch_one<128>(p, num_ctas, stream, pdl);
-    case 240: return launch_one<240>(p, num_ctas, stream, pdl);
-    case 256: return launch_one<256>(p, num_ctas, stream, pdl);
+    case 16: return launch_one<16, false>(p, num_ctas, stream, pdl);
+    case 32: return launch_one<32, false>(p, num_ctas, stream, pdl);
+    case 64: return launch_one<64, false>(p, num_ctas, stream, pdl);
+    case 128: return launch_one<128, false>(p, num_ctas, stream, pdl);
+    case 240: return launch_one<240, false>(p, num_ctas, stream, pdl);
+    case 256: return launch_one<256, false>(p, num_ctas, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

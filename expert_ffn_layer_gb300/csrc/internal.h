@@ -66,6 +66,11 @@ struct GemmParams {
   const int32_t *offsets;
   __nv_bfloat16 *act, *act_s;  // gate/up outputs: A_act [S][I], A_shared [T][Is]
   __nv_bfloat16 *y, *y_s;      // down outputs: y_sorted [S][H], y_shared [T][H]
+  // FP8 expert weights (q8 != 0): the weight maps above are uint8 maps of E4M3
+  // codes (box {64, 128, 1}, no swizzle) and these are the per-row fp32 scales
+  int q8;
+  const float *sc_g, *sc_u, *sc_d;     // [E][I], [E][I], [E][H]
+  const float *sc_sg, *sc_su, *sc_sd;  // [Is], [Is], [H]
   unsigned *err;               // workspace error word
   unsigned *sync;              // workspace header: tile claim counter, exit counter, per-segment done counts
   int T, H, E, I, Is, top_k, S, has_shared;
@@ -88,6 +93,12 @@ struct CombineParams {
   int T, H, top_k, S;
 };
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream, bool pdl);
+
+// ------------------------------------------------------------------- FP8
+// codes [rows][cols] uint8 (E4M3) and scale [rows] fp32 of a bf16 [rows][cols]
+// matrix, one scale per row; cols a multiple of 8, pointers 16-byte aligned
+cudaError_t launch_quantize_rows(const __nv_bfloat16 *src, uint8_t *q, float *scale, long long rows, int cols,
+                                 cudaStream_t stream);
 
 // self-test: a bounded wait on a barrier nothing completes (records MOE_DEVERR_TIMEOUT)
 cudaError_t launch_wait_timeout(unsigned *err, unsigned long long limit_ns, cudaStream_t stream);

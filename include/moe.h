@@ -229,6 +229,46 @@ moe_status moe_fused_moe(const moe_dims *d, const moe_bf16 *hidden, const int32_
                          const moe_bf16 *w_gate_up, const moe_bf16 *w_down, const moe_bf16 *ws_gate_up,
                          const moe_bf16 *ws_down, moe_bf16 *out, void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------ FP8
+ * FP8 expert weights (next step of the survey's plan; [case] lists W8A8
+ * quantised deployments and quantises inside the FusedMoE chain, but fixes no
+ * format).  Reading: every expert matrix row (an output feature) is stored as
+ * OCP E4M3 codes plus one fp32 scale, scale = max|row| / 448 (1 for a zero
+ * row), code = E4M3 round-to-nearest-even of w / scale, saturated at 448.  The
+ * layer uses value(code) * scale as the weight: the expert kernel feeds the
+ * code values (exact in bf16) to the MMAs and multiplies each row's fp32
+ * accumulator by its scale.  Activations stay bf16 (weight-only quantisation:
+ * it halves the weight bytes that bound decode). */
+typedef struct {
+  const uint8_t *gate, *up;                 /* [E, I, H] E4M3 codes */
+  const uint8_t *down;                      /* [E, H, I] */
+  const float *gate_scale, *up_scale;       /* [E, I] fp32, one per row */
+  const float *down_scale;                  /* [E, H] */
+  const uint8_t *s_gate, *s_up;             /* shared expert [I_shared, H] (unused when !has_shared) */
+  const uint8_t *s_down;                    /* [H, I_shared] */
+  const float *s_gate_scale, *s_up_scale;   /* [I_shared] */
+  const float *s_down_scale;                /* [H] */
+} moe_fp8_experts;
+
+/* Quantise a bf16 matrix [rows, cols] (cols a multiple of 8) row by row:
+ * codes [rows, cols] uint8 and scales [rows] fp32 as described above.  Pointers
+ * 16-byte aligned (scales 4-byte).  Async on `stream`. */
+moe_status moe_quantize_fp8_rows(const moe_bf16 *src, int64_t rows, int cols, uint8_t *codes, float *scales,
+                                 void *stream);
+
+/* moe_expert_ffn with FP8 expert weights (all pointers in *w 16-byte aligned).
+ * The FP8 kernel runs tiles of at most 128 tokens; results, layouts and errors
+ * as for moe_expert_ffn. */
+moe_status moe_expert_ffn_fp8(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
+                              const int32_t *offsets, const moe_fp8_experts *w, moe_bf16 *y_sorted,
+                              moe_bf16 *y_shared, void *ws, size_t ws_bytes, void *stream);
+
+/* moe_layer_forward with FP8 expert weights: moe_route, moe_permute,
+ * moe_expert_ffn_fp8, moe_combine on `stream`, intermediates in `ws`. */
+moe_status moe_layer_forward_fp8(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
+                                 const float *expert_bias, const moe_fp8_experts *w, moe_bf16 *out, void *ws,
+                                 size_t ws_bytes, void *stream);
+
 /* The whole layer (a1-a9) chained on `stream` with programmatic dependent
  * launch; every intermediate lives in `ws`.  Arguments as above; out [T, H] bf16. */
 moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,

@@ -21,7 +21,7 @@ def lib():
 def _declared_functions():
     text = (ROOT / "include" / "moe.h").read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):
@@ -81,6 +81,16 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
     assert lib.moe_combine(byref(d), None, None, None, None, None, None) == 1
     assert lib.moe_layer_forward(byref(d), *([None] * 11), 0, None) == 1
     assert lib.moe_fused_moe(byref(d), *([None] * 9), 0, None) == 1
+    assert lib.moe_expert_ffn_fp8(byref(d), None, None, None, None, None, None, None, 0, None) == 1
+    assert lib.moe_layer_forward_fp8(byref(d), None, None, None, None, None, None, 0, None) == 1
+    assert lib.moe_quantize_fp8_rows(None, 4, 12, None, None, None) == 1      # cols % 8
+    assert lib.moe_quantize_fp8_rows(None, 0, 16, None, None, None) == 0      # nothing to do
+    # an FP8 weight struct with a missing scale array is rejected before launch
+    fp8 = moe.MoeFp8Experts(gate=0x100000, up=0x100000, down=0x100000, gate_scale=0x100000, up_scale=None,
+                            down_scale=0x100000, s_gate=0x100000, s_up=0x100000, s_down=0x100000,
+                            s_gate_scale=0x100000, s_up_scale=0x100000, s_down_scale=0x100000)
+    g = 0x100000
+    assert lib.moe_expert_ffn_fp8(byref(d), g, g, g, byref(fp8), g, g, g, 1 << 40, None) == 1
     # misaligned pointer (never dereferenced: validation fails first)
     bad = 0x1003
     assert lib.moe_combine(byref(d), bad, bad, bad, bad, bad, None) == 1
