@@ -414,6 +414,54 @@ def run_ours(args, rank, world, local_rank):
         "kernels": kernels,
         "clocks": clk.summary(),
     }
+    # ---------------- the same decode layer with FP8 (E4M3, one scale per row)
+    # expert weights: quantised once on the device, then moe_layer_forward_fp8
+    # as a graph; not the headline (the metric names bf16 weights)
+    if world == 1 and not args.no_fp8:
+        try:
+            fp8 = moe.quantize_fp8_experts(layer.w_gate, layer.w_up, layer.w_down, layer.ws_gate, layer.ws_up,
+                                           layer.ws_down)
+            fout = torch.empty_like(out)
+
+            def fp8_step():
+                moe.moe_layer_forward_fp8(d, hidden, layer.router_w, layer.expert_bias, fp8, fout, layer.ws)
+
+            fgraph = graph_of(fp8_step, 1)
+            fms = float(np.sum(timed(fgraph.replay, args.steps, args.warmup))) / args.steps
+            ferr = moe.moe_ws_read_error(layer.ws)
+            S = w.T * w.top_k
+            perm_s = torch.empty(S, dtype=torch.int32, device=dev)
+            offs_s = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+            idx_s = torch.empty((w.T, w.top_k), dtype=torch.int32, device=dev)
+            wts_s = torch.empty((w.T, w.top_k), dtype=torch.float32, device=dev)
+            moe.moe_route(d, hidden, layer.router_w, layer.expert_bias, idx_s, wts_s, layer.ws)
+            moe.moe_permute(d, idx_s, torch.empty(w.E, dtype=torch.int32, device=dev), offs_s, perm_s,
+                            torch.empty(S, dtype=torch.int32, device=dev), layer.ws)
+            y_s = torch.empty((S, w.H), dtype=torch.bfloat16, device=dev)
+            z_s = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+            eg = graph_of(lambda: moe.moe_expert_ffn_fp8(d, hidden, perm_s, offs_s, fp8, y_s, z_s, layer.ws),
+                          args.steps)
+            eg.replay()
+            flush_l2(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            eg.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ems = e0.elapsed_time(e1) / args.steps
+            wbytes = (n_active * 3 * w.I + 3 * w.I_shared) * w.H          # one byte per code
+            sbytes = (n_active * (2 * w.I + w.H) + 2 * w.I_shared + w.H) * 4
+            result["fp8_decode"] = {
+                "weights": "E4M3 codes, one fp32 scale per output row (moe_quantize_fp8_rows)",
+                "value": round(w.T / (fms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(fms, 5),
+                "expert_ffn_ms": round(ems, 4),
+                "expert_ffn_code_bytes": wbytes + sbytes,
+                "expert_ffn_gbs": round((wbytes + sbytes) / (ems * 1e-3) / 1e9, 1),
+                "device_error": ferr,
+            }
+            del fp8, fgraph, eg
+        except Exception as e:  # an auxiliary measurement: record the failure, keep the headline
+            result["fp8_decode"] = {"error": f"{type(e).__name__}: {e}"}
     del layer, hidden, layer_graph
     torch.cuda.empty_cache()
 
@@ -561,6 +609,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the skewed long-prefill (T=16384) and HunyuanImage (T=8192) measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-weight decode measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:
