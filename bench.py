@@ -340,10 +340,16 @@ def run_ours(args, rank, world, local_rank):
     w, d, layer, hidden, hidden_np, host = setup(name, rank)
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
     if args.profile:
-        for _ in range(args.warmup + 1):
-            layer(hidden, out)
+        if args.fp8:  # the same layer with FP8 expert weights (quantised once, before the layers)
+            q = moe.quantize_fp8_experts(layer.w_gate, layer.w_up, layer.w_down, layer.ws_gate, layer.ws_up,
+                                         layer.ws_down)
+            for _ in range(args.warmup + 1):
+                moe.moe_layer_forward_fp8(d, hidden, layer.router_w, layer.expert_bias, q, out, layer.ws)
+        else:
+            for _ in range(args.warmup + 1):
+                layer(hidden, out)
         torch.cuda.synchronize()
-        return {"profile": name, "device_error": moe.moe_ws_read_error(layer.ws)}
+        return {"profile": name, "fp8": bool(args.fp8), "device_error": moe.moe_ws_read_error(layer.ws)}
 
     def eager_step():
         layer(hidden, out)
@@ -610,6 +616,7 @@ def main():
                     help="skip the skewed long-prefill (T=16384) and HunyuanImage (T=8192) measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-weight decode measurement")
+    ap.add_argument("--fp8", action="store_true", help="with --profile: run the layer with FP8 expert weights")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:
