@@ -114,3 +114,38 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         moe.load()
     importlib.reload(moe)
+
+
+def _c_struct_fields(typedef_name):
+    """(name, C type) of each field of `typedef struct { ... } typedef_name;` in
+    moe.h, in declaration order (comments stripped; 'T, H, E' style lists split)."""
+    text = re.sub(r"/\*.*?\*/", "", (ROOT / "include" / "moe.h").read_text(), flags=re.S)
+    m = re.search(r"typedef struct \{([^{}]*)\}\s*" + typedef_name + r"\s*;", text)
+    assert m, typedef_name
+    fields = []
+    for decl in m.group(1).split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        ctype, names = re.match(r"((?:const\s+)?[a-z0-9_]+\s*\**)\s*(.*)", decl).groups()
+        for n in names.split(","):
+            n = n.strip()
+            stars = n.count("*")
+            fields.append((n.lstrip("*").strip(), ctype.replace(" ", "") + "*" * stars))
+    return fields
+
+
+def test_binding_structs_match_the_header():
+    """The ctypes mirrors of moe_dims and moe_fp8_experts have the header's
+    fields in the header's order, with matching scalar kinds (a reordered or
+    retyped field would silently pass the wrong value)."""
+    dims = _c_struct_fields("moe_dims")
+    assert [n for n, _ in dims] == [n for n, _ in moe.MoeDims._fields_]
+    kinds = {"int": ctypes.c_int, "float": ctypes.c_float}
+    for (n, t), (bn, bt) in zip(dims, moe.MoeDims._fields_):
+        assert kinds[t] is bt, (n, t, bt)
+    fp8 = _c_struct_fields("moe_fp8_experts")
+    assert [n for n, _ in fp8] == [n for n, _ in moe.MoeFp8Experts._fields_]
+    assert all(t.endswith("*") for _, t in fp8)                 # every field a pointer
+    assert all(bt is ctypes.c_void_p for _, bt in moe.MoeFp8Experts._fields_)
+    assert ctypes.sizeof(moe.MoeFp8Experts) == len(fp8) * ctypes.sizeof(ctypes.c_void_p)
