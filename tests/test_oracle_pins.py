@@ -202,6 +202,83 @@ def test_near_tie_alternatives():
     assert cand[0].tolist() == [False, True, True, False, True]
 
 
+# ------------------------------------------- a given selection (near-tie rows)
+# The GPU parity tests grade a near-tie row against the oracle re-evaluated with
+# the GPU's selection (layer_forward(topk_idx=...)); these pins tie that path to
+# hand-worked weights, so a wrong weight rule for a given selection fails here.
+
+def _override_cases(golden_dir):
+    return _golden(golden_dir, "routing_worked_example.json")["override_cases"]
+
+
+def _one_token_layer(case, seed=31, I=3, Is=2):
+    """One token whose router logits are the case's logits: H = 1, hidden [[1.0]]
+    (bf16 0x3F80) and a one-column fp32 router weight holding the logits."""
+    E = len(case["logits"])
+    x = np.array([[0x3F80]], dtype=np.uint16)
+    wr = np.array(case["logits"], dtype=np.float32)[:, None]
+    bias = np.array(case["bias"], dtype=np.float32) if case["mode"] == "sigmoid" else None
+    wg = W.normal_bf16(seed, 4, (E, I, 1), 0.7)
+    wu = W.normal_bf16(seed, 5, (E, I, 1), 0.7)
+    wd = W.normal_bf16(seed, 6, (E, 1, I), 0.7)
+    sg = W.normal_bf16(seed, 7, (Is, 1), 0.7)
+    su = W.normal_bf16(seed, 8, (Is, 1), 0.7)
+    sd = W.normal_bf16(seed, 9, (1, Is), 0.7)
+    return x, wr, bias, wg, wu, wd, sg, su, sd
+
+
+def _run_case(case, inputs, topk_idx=None):
+    return oracle.layer_forward(*inputs, top_k=case["k"], score_mode=case["mode"], route_scale=case["route_scale"],
+                                renorm_eps=case["eps"], topk_idx=topk_idx)
+
+
+def test_given_selection_weights_hand_worked(golden_dir):
+    """A valid alternative selection gets the weights the routing rule gives that
+    set: the unbiased sigmoids renormalised and scaled (sigmoid rule), or the
+    softmax mass over clamp(sum, eps) (softmax rule) -- not the biased keys, not
+    the unscaled sum, not the unclamped sum."""
+    for case in _override_cases(golden_dir):
+        inputs = _one_token_layer(case)
+        own = _run_case(case, inputs)
+        assert own["idx"][0].tolist() == case["own_idx"], case["note"]
+        np.testing.assert_allclose(own["w"][0], case["own_w"], rtol=1e-6)
+        # the alternative is a valid near-tie choice under the 1e-5 rule
+        mand, cand = oracle.near_tie_alternatives(own["keys"], case["k"], 1e-5)
+        alt = set(case["alt_idx"])
+        assert set(np.nonzero(mand[0])[0]) <= alt <= set(np.nonzero(mand[0] | cand[0])[0])
+        r = _run_case(case, inputs, topk_idx=np.array([case["alt_idx"]], dtype=np.int32))
+        assert r["idx"][0].tolist() == case["alt_idx"]
+        np.testing.assert_allclose(r["w"][0], case["alt_w"], rtol=1e-6)
+
+
+def test_given_selection_layer_matches_per_token_brute_force(golden_dir):
+    """The layer output for the alternative selection equals a direct per-token
+    sum of the chosen experts' SwiGLU outputs with the hand-worked weights, plus
+    the shared expert."""
+    f = W.bf16_to_f64
+    for case in _override_cases(golden_dir):
+        inputs = _one_token_layer(case)
+        x, _, _, wg, wu, wd, sg, su, sd = inputs
+        r = _run_case(case, inputs, topk_idx=np.array([case["alt_idx"]], dtype=np.int32))
+        out = _dense_swiglu_loops(f(x), f(sg), f(su), f(sd))[0]
+        for e, w in zip(case["alt_idx"], case["alt_w"]):
+            out = out + w * _dense_swiglu_loops(f(x), f(wg[e]), f(wu[e]), f(wd[e]))[0]
+        np.testing.assert_allclose(r["out"][0], out, rtol=1e-6, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", ["sigmoid", "softmax"])
+def test_given_own_selection_is_the_default_call(mode):
+    """Passing the oracle's own selection back in changes nothing, bit for bit."""
+    T, H, E, k, I, Is = 9, 8, 6, 3, 4, 5
+    x, wr, b, wg, wu, wd, sg, su, sd = _tiny_layer_inputs(24, T, H, E, I, Is)
+    kw = dict(top_k=k, score_mode=mode, route_scale=2.826 if mode == "sigmoid" else 1.0,
+              renorm_eps=0.0 if mode == "sigmoid" else 1e-8)
+    r = oracle.layer_forward(x, wr, b, wg, wu, wd, sg, su, sd, **kw)
+    r2 = oracle.layer_forward(x, wr, b, wg, wu, wd, sg, su, sd, topk_idx=r["idx"], **kw)
+    for key in ("idx", "w", "perm", "inv", "out"):
+        assert np.array_equal(r[key], r2[key]), key
+
+
 # --------------------------------------------------------- histogram / permutation
 
 def test_permutation_brute_force_and_invariants():
