@@ -35,7 +35,7 @@ SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
 EXPORTS = ("moe_status_string", "moe_check_dims", "moe_workspace_bytes", "moe_ws_init", "moe_ws_read_error",
            "moe_route", "moe_permute", "moe_expert_ffn", "moe_expert_gate_up", "moe_expert_down", "moe_combine",
            "moe_layer_forward", "moe_fused_moe", "moe_expert_ffn_noalloc", "moe_selftest_wait_timeout",
-           "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_layer_forward_fp8")
+           "moe_selftest_silu", "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_layer_forward_fp8")
 
 
 class MoeError(RuntimeError):
@@ -96,6 +96,7 @@ def load() -> ctypes.CDLL:
         "moe_expert_ffn_fp8": (st, [D, P, P, P, ctypes.POINTER(MoeFp8Experts), P, P, P, C, P]),
         "moe_layer_forward_fp8": (st, [D, P, P, P, ctypes.POINTER(MoeFp8Experts), P, P, C, P]),
         "moe_selftest_wait_timeout": (st, [P, C, ctypes.c_ulonglong, P]),
+        "moe_selftest_silu": (st, [P, P, P, ctypes.c_int64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -363,6 +364,15 @@ def moe_layer_forward_fp8(d: MoeDims, hidden, router_w, expert_bias, w: Fp8Exper
 
 def moe_selftest_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> None:
     _call("moe_selftest_wait_timeout", _ptr(ws), ws.numel(), limit_ns, _stream(stream))
+
+
+def moe_selftest_silu(g, u, out, stream=None) -> None:
+    """out = the expert epilogue's SiLU(g) * u, element-wise (fp32 device tensors)."""
+    n = g.numel()
+    _check(g, torch.float32, (n,), "g")
+    _check(u, torch.float32, (n,), "u")
+    _check(out, torch.float32, (n,), "out")
+    _call("moe_selftest_silu", _ptr(g), _ptr(u), _ptr(out), n, _stream(stream))
 
 
 class MoELayer:

@@ -425,6 +425,14 @@ MOE_API moe_status moe_selftest_wait_timeout(void *ws, size_t ws_bytes, unsigned
   return cuda_status(launch_wait_timeout(at<unsigned>(ws, 0), limit_ns, (cudaStream_t)stream));
 }
 
+MOE_API moe_status moe_selftest_silu(const float *g, const float *u, float *out, int64_t n, void *stream) {
+  if (n < 0) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  auto f32_ok = [](const float *p) { return p != nullptr && ((uintptr_t)p & 3u) == 0; };
+  if (!f32_ok(g) || !f32_ok(u) || !f32_ok(out)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_silu_selftest(g, u, out, (long long)n, (cudaStream_t)stream));
+}
+
 MOE_API moe_status moe_route(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
                              const float *expert_bias, float *logits_out, int32_t *topk_idx, float *topk_w, void *ws,
                              size_t ws_bytes, void *stream) {

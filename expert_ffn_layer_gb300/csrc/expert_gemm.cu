@@ -57,6 +57,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "silu.cuh"
 
 namespace moe {
 
@@ -208,26 +209,6 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// SiLU(g) * u = g * u / (1 + e^-g) with one special-function operation per
-// element (the epilogue of a 256-token tile is bound by them): e^-g =
-// 2^(-g log2 e) by the hardware base-2 exponential (argument capped at 120 so
-// the denominator stays a normal float), then 1/d by Newton's iteration
-// r <- r (2 - d r) from a bit-pattern seed.  The seed K - bits(d) with
-// K = 0x7EF311C0 (the constant that minimises its worst relative error, 5.1 %,
-// over a binade) reaches 6.5e-6 after two steps; with the exponential's error
-// the result is within 9e-6 of SiLU(g) * u relative -- far below the bf16
-// rounding that follows.  For g < -83 the true value is below 1e-34.
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  const float x = fminf(-1.4426950409f * g, 120.0f);
-  float e;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x));
-  const float d = 1.0f + e;
-  float r = __int_as_float(0x7EF311C0 - __float_as_int(d));
-  r = r * fmaf(-d, r, 2.0f);
-  r = r * fmaf(-d, r, 2.0f);
-  return g * u * r;
 }
 
 // Eight E4M3 codes (two little-endian words, first code in the low byte) to the

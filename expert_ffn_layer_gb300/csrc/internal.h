@@ -102,6 +102,8 @@ cudaError_t launch_quantize_rows(const __nv_bfloat16 *src, uint8_t *q, float *sc
 
 // self-test: a bounded wait on a barrier nothing completes (records MOE_DEVERR_TIMEOUT)
 cudaError_t launch_wait_timeout(unsigned *err, unsigned long long limit_ns, cudaStream_t stream);
+// self-test: out[i] = the expert epilogue's SiLU(g[i]) * u[i], n >= 1
+cudaError_t launch_silu_selftest(const float *g, const float *u, float *out, long long n, cudaStream_t stream);
 
 // shared launch helper: PDL attribute on, optional cluster dims
 cudaError_t launch_ex(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,

@@ -119,6 +119,13 @@ moe_status moe_ws_read_error(void *ws, size_t ws_bytes, int clear, void *stream,
  * same way (1 s), so a broken pipeline reports an error instead of hanging. */
 moe_status moe_selftest_wait_timeout(void *ws, size_t ws_bytes, unsigned long long limit_ns, void *stream);
 
+/* Self-test of step a6's arithmetic: out[i] = SiLU(g[i]) * u[i] computed by the
+ * same device function the expert kernel's gate/up epilogue uses (a hardware
+ * base-2 exponential and a Newton-Raphson reciprocal), so that its error can be
+ * measured against a float64 reference.  g, u, out: [n] fp32 device arrays,
+ * 4-byte aligned; n >= 0 (0 is a no-op).  Async on `stream`. */
+moe_status moe_selftest_silu(const float *g, const float *u, float *out, int64_t n, void *stream);
+
 /* Steps a1-a2: router GEMM and routing.  [case] section 2; [hy3] MoE routing;
  * [image] easy_topk.
  *   hidden      [T, H] bf16 row-major (input)
