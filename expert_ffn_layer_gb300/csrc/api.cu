@@ -40,6 +40,39 @@ cudaError_t launch_ex(const void *func, dim3 grid, dim3 block, size_t smem, cuda
   return cudaLaunchKernelExC(&cfg, func, args);
 }
 
+unsigned long long context_id() {
+  using GetCurrent = CUresult (*)(CUcontext *);
+  using GetId = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+cudaError_t set_smem_attr_once(const void *func, int bytes, unsigned long long &done_ctx) {
+  const unsigned long long ctx = context_id();
+  if (ctx != 0 && ctx == done_ctx) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  // the call above makes the primary context current if none was: look again
+  if (e == cudaSuccess) done_ctx = ctx != 0 ? ctx : context_id();
+  return e;
+}
+
 namespace {
 
 // ------------------------------------------------------------ tensor maps
@@ -225,6 +258,19 @@ moe_status do_permute(const moe_dims &d, const int32_t *topk_idx, int32_t *count
   return cuda_status(launch_permute(p, stream, pdl));
 }
 
+// The expert kernel's scratch: the workspace header (error word, tile-claim and
+// completion counters) and the bf16 activations between gate/up and down.
+struct ExpertScratch {
+  unsigned *hdr;
+  __nv_bfloat16 *act, *act_s;
+};
+
+// the scratch inside a caller's workspace (moe_workspace_bytes layout)
+ExpertScratch scratch_in(const moe_dims &d, void *ws) {
+  const WsLayout L = ws_layout(d);
+  return {at<unsigned>(ws, L.err), at<__nv_bfloat16>(ws, L.a_act), at<__nv_bfloat16>(ws, L.a_shared)};
+}
+
 // Tensor maps and pointers of the grouped expert FFN; `phases` selects gate/up
 // (1), down (2) or both in one persistent launch (3).  gu_stride: rows from one
 // expert's gate (up) matrix to the next's -- I for separate [E, I, H] tensors,
@@ -232,10 +278,9 @@ moe_status do_permute(const moe_dims &d, const int32_t *topk_idx, int32_t *count
 moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidden, const int32_t *perm,
                             const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
                             const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
-                            const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws,
-                            cudaStream_t stream, bool pdl, uint64_t gu_stride = 0,
+                            const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared,
+                            const ExpertScratch &sc, cudaStream_t stream, bool pdl, uint64_t gu_stride = 0,
                             const moe_fp8_experts *q = nullptr) {
-  const WsLayout L = ws_layout(d);
   GemmParams g;
   std::memset(&g, 0, sizeof(g));
   g.T = d.T;
@@ -250,10 +295,10 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
   g.hidden = reinterpret_cast<const __nv_bfloat16 *>(hidden);
   g.perm = perm;
   g.offsets = offsets;
-  g.err = at<unsigned>(ws, L.err);
-  g.sync = at<unsigned>(ws, L.err);
-  g.act = at<__nv_bfloat16>(ws, L.a_act);
-  g.act_s = at<__nv_bfloat16>(ws, L.a_shared);
+  g.err = sc.hdr;
+  g.sync = sc.hdr;
+  g.act = sc.act;
+  g.act_s = sc.act_s;
   g.y = reinterpret_cast<__nv_bfloat16 *>(y_sorted);
   g.y_s = reinterpret_cast<__nv_bfloat16 *>(y_shared);
   bool ok = true;
@@ -299,14 +344,14 @@ moe_status do_gate_up(const moe_dims &d, const moe_bf16 *hidden, const int32_t *
                       const moe_bf16 *w_gate, const moe_bf16 *w_up, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
                       void *ws, cudaStream_t stream, bool pdl) {
   return do_expert_phases(d, 1, hidden, perm, offsets, w_gate, w_up, nullptr, ws_gate, ws_up, nullptr, nullptr,
-                          nullptr, ws, stream, pdl);
+                          nullptr, scratch_in(d, ws), stream, pdl);
 }
 
 // a7-a8: down GEMM over the activations in ws -> y_sorted, y_shared
 moe_status do_down(const moe_dims &d, const int32_t *offsets, const moe_bf16 *w_down, const moe_bf16 *ws_down,
                    moe_bf16 *y_sorted, moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl) {
   return do_expert_phases(d, 2, nullptr, nullptr, offsets, nullptr, nullptr, w_down, nullptr, nullptr, ws_down,
-                          y_sorted, y_shared, ws, stream, pdl);
+                          y_sorted, y_shared, scratch_in(d, ws), stream, pdl);
 }
 
 // a5-a8 in one persistent launch
@@ -315,7 +360,7 @@ moe_status do_expert_ffn(const moe_dims &d, const moe_bf16 *hidden, const int32_
                          const moe_bf16 *ws_gate, const moe_bf16 *ws_up, const moe_bf16 *ws_down, moe_bf16 *y_sorted,
                          moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl) {
   return do_expert_phases(d, 3, hidden, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_sorted,
-                          y_shared, ws, stream, pdl);
+                          y_shared, scratch_in(d, ws), stream, pdl);
 }
 
 moe_status do_combine(const moe_dims &d, const moe_bf16 *y_sorted, const moe_bf16 *y_shared, const int32_t *inv,
@@ -358,7 +403,8 @@ moe_status do_fused_moe(const moe_dims &d, const moe_bf16 *hidden, const int32_t
   if (st != MOE_OK) return st;
   const size_t up = (size_t)d.I * d.H, sup = d.has_shared ? (size_t)d.I_shared * d.H : 0;
   st = do_expert_phases(d, 3, hidden, perm, offs, w_gate_up, w_gate_up + up, w_down, ws_gate_up,
-                        d.has_shared ? ws_gate_up + sup : nullptr, ws_down, y, z, ws, s, true, 2 * (uint64_t)d.I);
+                        d.has_shared ? ws_gate_up + sup : nullptr, ws_down, y, z, scratch_in(d, ws), s, true,
+                        2 * (uint64_t)d.I);
   if (st != MOE_OK) return st;
   return do_combine(d, y, z, inv, topk_w, out, s, true);
 }
@@ -553,7 +599,7 @@ MOE_API moe_status moe_expert_ffn_fp8(const moe_dims *d, const moe_bf16 *hidden,
   if (d->has_shared && !ptr_ok(y_shared)) return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
   return do_expert_phases(*d, 3, hidden, perm, offsets, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                          y_sorted, y_shared, ws, (cudaStream_t)stream, true, 0, w);
+                          y_sorted, y_shared, scratch_in(*d, ws), (cudaStream_t)stream, true, 0, w);
 }
 
 MOE_API moe_status moe_layer_forward_fp8(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
@@ -575,7 +621,7 @@ MOE_API moe_status moe_layer_forward_fp8(const moe_dims *d, const moe_bf16 *hidd
   if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, wt, ws, s, true)) != MOE_OK) return st;
   if ((st = do_permute(*d, idx, at<int32_t>(ws, L.counts), offs, perm, inv, ws, s, true)) != MOE_OK) return st;
   if ((st = do_expert_phases(*d, 3, hidden, perm, offs, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, y, z,
-                             ws, s, true, 0, w)) != MOE_OK)
+                             scratch_in(*d, ws), s, true, 0, w)) != MOE_OK)
     return st;
   return do_combine(*d, y, z, inv, wt, out, s, true);
 }
@@ -610,36 +656,55 @@ MOE_API moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, 
 
 // ---------------------------------------------------------------------------
 // moe_expert_ffn_noalloc: moe_expert_ffn for callers that cannot allocate
-// device memory.  Its scratch (the error word and the bf16 activations between
-// the gate/up and the down GEMM) lives in the file-scope array below instead
-// of a caller-provided workspace.
+// device memory.  Its scratch (the error word and tile counters, and the bf16
+// activations between the gate/up and the down GEMM) lives in the file-scope
+// array below instead of a caller-provided workspace, laid out compactly:
+// header, then the routed activations [T * top_k, I], then the shared ones [T, I_shared].
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB, held on every device that loads this library
 __device__ __align__(256) static unsigned char g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_scratch_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+struct NoallocLayout {
+  size_t act, act_s, total;
+};
+NoallocLayout noalloc_layout(const moe_dims &d) {
+  NoallocLayout L;
+  const size_t S = (size_t)d.T * d.top_k;
+  L.act = align256(kWsHeaderBytes);
+  L.act_s = align256(L.act + S * (size_t)d.I * 2);
+  L.total = L.act_s + (d.has_shared ? (size_t)d.T * d.I_shared * 2 : 0);
+  return L;
+}
 
-// Device address of the array on the current device (the host-side name is not
-// one).  Looked up once per device, on that device's first call.
+// Device address of the array in the current context (the host-side name is
+// not one), looked up with cudaGetSymbolAddress on a context's first call and
+// cached under the context's unique id, so that a new context on the same
+// device (after cudaDeviceReset, or one the caller made current) gets its own.
+constexpr int kScratchCache = 16;
+std::mutex g_scratch_mutex;
+struct {
+  unsigned long long ctx;
+  void *ptr;
+} g_scratch_cache[kScratchCache] = {};
+int g_scratch_next = 0;
+
 void *static_scratch(cudaError_t *err) {
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= kMaxDevices) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
+  *err = cudaSuccess;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void *p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = p;
+  unsigned long long ctx = context_id();
+  if (ctx != 0)
+    for (auto &c : g_scratch_cache)
+      if (c.ctx == ctx) return c.ptr;
+  void *p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_static_scratch);  // makes the primary context current if none was
+  if (*err != cudaSuccess) return nullptr;
+  if (ctx == 0) ctx = context_id();
+  if (ctx != 0) {
+    g_scratch_cache[g_scratch_next] = {ctx, p};
+    g_scratch_next = (g_scratch_next + 1) % kScratchCache;
   }
-  return g_scratch_ptr[dev];
+  return p;
 }
 
 }  // namespace
@@ -657,14 +722,16 @@ MOE_API moe_status moe_expert_ffn_noalloc(const moe_dims *d, const moe_bf16 *hid
     return MOE_ERR_INVALID_ARG;
   if (d->has_shared && (!ptr_ok(ws_gate) || !ptr_ok(ws_up) || !ptr_ok(ws_down) || !ptr_ok(y_shared)))
     return MOE_ERR_INVALID_ARG;
-  if (ws_layout(*d).total > kStaticScratchBytes) return MOE_ERR_WORKSPACE;  // beyond the built-in scratch
+  const NoallocLayout L = noalloc_layout(*d);
+  if (L.total > kStaticScratchBytes) return MOE_ERR_WORKSPACE;  // beyond the built-in scratch
   cudaError_t e = cudaSuccess;
-  void *ws = static_scratch(&e);
-  if (ws == nullptr) return MOE_ERR_CUDA;
+  void *base = static_scratch(&e);
+  if (base == nullptr) return MOE_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   // the array keeps the previous call's contents: the header (error word and
   // tile-scheduler counters) must start at zero
-  if (cudaMemsetAsync(ws, 0, kWsHeaderBytes, s) != cudaSuccess) return MOE_ERR_CUDA;
-  return do_expert_ffn(*d, hidden, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_sorted, y_shared,
-                       ws, s, true);
+  if (cudaMemsetAsync(base, 0, kWsHeaderBytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const ExpertScratch sc = {at<unsigned>(base, 0), at<__nv_bfloat16>(base, L.act), at<__nv_bfloat16>(base, L.act_s)};
+  return do_expert_phases(*d, 3, hidden, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_sorted,
+                          y_shared, sc, s, true);
 }

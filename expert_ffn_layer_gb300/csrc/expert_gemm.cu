@@ -842,15 +842,9 @@ namespace {
 template <int BN, bool Q8>
 cudaError_t launch_one(const GemmParams &p, int num_ctas, cudaStream_t stream, bool pdl) {
   using L = Layout<BN, Q8>;
-  static thread_local int configured_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    cudaError_t e =
-        cudaFuncSetAttribute(expert_ffn_kernel<BN, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmem);
-    if (e != cudaSuccess) return e;
-    configured_dev = dev;
-  }
+  static thread_local unsigned long long attr_ctx = 0;
+  const cudaError_t e = set_smem_attr_once((const void *)expert_ffn_kernel<BN, Q8>, (int)L::kSmem, attr_ctx);
+  if (e != cudaSuccess) return e;
   void *args[] = {(void *)&p};
   return launch_ex((const void *)expert_ffn_kernel<BN, Q8>, dim3(num_ctas), dim3(kGemmThreads), L::kSmem, stream, pdl, 1,
                    args);

@@ -105,6 +105,17 @@ cudaError_t launch_wait_timeout(unsigned *err, unsigned long long limit_ns, cuda
 // self-test: out[i] = the expert epilogue's SiLU(g[i]) * u[i], n >= 1
 cudaError_t launch_silu_selftest(const float *g, const float *u, float *out, long long n, cudaStream_t stream);
 
+// Unique id of the CUDA context current on the calling thread (0 when none is
+// current yet).  Per-context state -- a kernel's shared-memory attribute, a
+// module symbol's device address -- is cached under it rather than under the
+// device ordinal: one ordinal names different contexts over a process's life
+// (after cudaDeviceReset, or when a caller makes its own context current
+// through the driver API).
+unsigned long long context_id();
+// cudaFuncSetAttribute(max dynamic shared memory) unless already done for the
+// current context by this thread (done_ctx is the caller's per-thread cache).
+cudaError_t set_smem_attr_once(const void *func, int bytes, unsigned long long &done_ctx);
+
 // shared launch helper: PDL attribute on, optional cluster dims
 cudaError_t launch_ex(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
                       int cluster_x, void **args);

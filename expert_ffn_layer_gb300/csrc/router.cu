@@ -330,15 +330,17 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const __grid_constant_
 
 cudaError_t launch_router(const RouterParams &p, const float *router_w, int ksplit, int mtiles, cudaStream_t stream,
                           bool pdl) {
-  static thread_local int configured_dev = -1, nsm = 0;
+  static thread_local unsigned long long attr_ctx = 0;
+  static thread_local int nsm_dev = -1, nsm = 0;
+  {
+    const cudaError_t e = set_smem_attr_once((const void *)router_gemm_kernel, kSmemLimit, attr_ctx);
+    if (e != cudaSuccess) return e;
+  }
   int dev = 0;
   cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    cudaError_t e =
-        cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (e != cudaSuccess) return e;
+  if (nsm_dev != dev) {
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    configured_dev = dev;
+    nsm_dev = dev;
   }
   {  // split
     const long long n8 = (long long)p.E * p.H / 8;

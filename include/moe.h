@@ -192,15 +192,20 @@ moe_status moe_expert_down(const moe_dims *d, const int32_t *offsets, const moe_
  * no counterpart on the pages: this is an interface convenience, not a step of
  * the layer.
  *   Arguments and results as for moe_expert_ffn (the caller still passes every
- *   input and output).  Dims whose moe_workspace_bytes() exceeds 32 MiB are
- *   rejected with MOE_ERR_WORKSPACE before anything is launched (for the Hy3
- *   shape that admits batches up to T = 241 tokens).
- *   The first call on a device looks up that device's address of the array
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   input and output).  The scratch holds a 4 KiB header and the bf16
+ *   activations, T * top_k * I + T * I_shared values; dims that need more than
+ *   32 MiB are rejected with MOE_ERR_WORKSPACE before anything is launched (for
+ *   the Hy3 shape that admits batches up to T = 1213 tokens).
+ *   The first call in a CUDA context looks up that context's address of the
+ *   array (cudaGetSymbolAddress) and caches it under the context's unique id;
+ *   make that first call before any stream capture.
  *   Every call uses the same array: calls that overlap on the device (two
  *   streams, or two host threads) race and give wrong results; serialise them.
- *   Device-side anomalies are not reported on this path (the error word is
- *   cleared at the start of every call). */
+ *   Device-side anomalies cannot be read back on this path: the error word lives
+ *   in the array and every call clears it.  After one (perm or offsets outside
+ *   their ranges, or a bounded wait that ran out) y_sorted and y_shared are
+ *   undefined; callers that need to detect it use moe_expert_ffn with a
+ *   workspace and moe_ws_read_error. */
 moe_status moe_expert_ffn_noalloc(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
                                   const int32_t *offsets, const moe_bf16 *w_gate, const moe_bf16 *w_up,
                                   const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,

@@ -4,6 +4,10 @@ array).  Its results must equal those of moe_expert_ffn, which takes a
 caller-allocated workspace, on every call: the array is shared between calls
 and keeps the previous call's contents."""
 import ctypes
+import json
+import subprocess
+import sys
+from pathlib import Path
 
 import numpy as np
 import pytest
@@ -33,12 +37,20 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode"])
+# A batch whose whole-layer workspace (with y_sorted [T * top_k, H]) is beyond
+# 32 MiB while the entry point's own scratch (header + activations) fits.
+BEYOND_LAYER_WS = W.Workload("noalloc_wide", 600, 4096, 16, 8, 256, 256, "sigmoid", 2.826, 0.0, True, "normal", 0.1,
+                             12)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "noalloc_wide"])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(name):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     f = _noalloc_fn()
-    w = W.WORKLOADS[name]
+    w = BEYOND_LAYER_WS if name == "noalloc_wide" else W.WORKLOADS[name]
+    if name == "noalloc_wide":
+        assert moe.moe_workspace_bytes(dims_of(w)) > 32 << 20
     inp = W.layer_inputs(w)
     ref = oracle.layer_forward(inp["hidden"], inp["router_w"], inp["bias"], inp["w_gate"], inp["w_up"],
                                inp["w_down"], inp["ws_gate"], inp["ws_up"], inp["ws_down"], top_k=w.top_k,
@@ -67,7 +79,22 @@ def test_noalloc_rejects_dims_beyond_its_scratch():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     f = _noalloc_fn()
-    d = dims_of(W.WORKLOADS["prefill"])  # needs ~1.7 GB of scratch, far beyond the built-in 32 MiB
+    d = dims_of(W.WORKLOADS["prefill"])  # its activations alone are ~113 MB, beyond the built-in 32 MiB
     p = ctypes.c_void_p(1 << 20)       # aligned and never dereferenced: the call fails before any launch
     rc = f(ctypes.byref(d), *([p] * 10), p, None)
     assert rc == 3, moe.status_string(rc)  # MOE_ERR_WORKSPACE
+
+
+def test_noalloc_in_two_contexts_of_one_device():
+    """The scratch array's device address belongs to a CUDA context, not to a
+    device ordinal: a process that makes two contexts of its own current in
+    turn gets correct results in each (a child process, so that the contexts it
+    creates and destroys are its own)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    _noalloc_fn()  # built
+    child = Path(__file__).with_name("noalloc_contexts_child.py")
+    r = subprocess.run([sys.executable, str(child)], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["ok"] and len(set(res["context_ids"])) == 2, res
