@@ -40,6 +40,10 @@ Readings where the pages are silent (each also listed in the design notes):
 * FP8 expert weights (the Hy3 case's W8A8 deployments, format unspecified):
   OCP E4M3 codes with one fp32 scale per output row, max|row| / 448, rounded
   to nearest-even and saturated at 448; the layer uses value * scale.
+* W8A8 (the case's "activation quantisation + Down GEMM"): every activation
+  matrix feeding an expert GEMM is quantised per row by the same rule, from its
+  own values -- the hidden state per token, the bf16 SiLU(gate) * up activation
+  per routed slot; the router stays fp32.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 against closed forms, hand-worked examples (``tests/golden/``), brute force on
@@ -71,4 +75,7 @@ from .moe import (  # noqa: F401
     e4m3_encode,
     quantize_rows_e4m3,
     dequantize_rows_e4m3,
+    quantized_matmul,
+    swiglu_w8a8,
+    layer_forward_w8a8,
 )

@@ -293,6 +293,77 @@ def dequantize_rows_e4m3(q, scale) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# W8A8: FP8 (E4M3) weights and FP8 activations
+# ---------------------------------------------------------------------------
+# The Hy3 case's FusedMoE chain quantises the activations right before the down
+# GEMM ("activation quantisation + Down GEMM") in its W8A8 deployments; the
+# pages fix no format or granularity.  The reading here: the weights as above
+# (E4M3 codes, one fp32 scale per output row), and every activation matrix that
+# feeds a GEMM quantised the same way per row, dynamically from its own values:
+# the hidden state per token before the gate/up GEMM, and the SiLU(gate) * up
+# activation per routed slot (per token for the shared expert) before the down
+# GEMM.  The activation the down GEMM quantises is the bf16 value the layer
+# stores between the two GEMMs.  Products of two codes are exact, so each
+# output element is (sum of code products) * row scale * column scale.  The
+# router is not quantised (it stays in fp32).
+
+
+def quantized_matmul(xq, xs, wq, ws) -> np.ndarray:
+    """out[t, o] = sum_h value(xq[t, h]) * value(wq[o, h]) * xs[t] * ws[o]: an
+    nn.Linear whose input rows and weight rows are both E4M3 codes with one
+    scale per row."""
+    acc = e4m3_value(xq) @ e4m3_value(wq).T
+    return acc * np.asarray(xs, dtype=np.float64)[:, None] * np.asarray(ws, dtype=np.float64)[None, :]
+
+
+def swiglu_w8a8(xq, xs, g, u, d) -> np.ndarray:
+    """One SwiGLU expert, W8A8: gate and up from the quantised input rows, the
+    activation a = SiLU(gate) * up stored as bf16 and quantised per row, then the
+    down projection.  g, u, d are (codes, scales) pairs of the three weights."""
+    gate = quantized_matmul(xq, xs, *g)
+    up = quantized_matmul(xq, xs, *u)
+    a = bf16_round(silu(gate) * up)
+    aq, a_s = quantize_rows_e4m3(a)
+    return quantized_matmul(aq, a_s, *d)
+
+
+def layer_forward_w8a8(hidden, router_w, bias, experts, shared, *, top_k: int, score_mode: str = "sigmoid",
+                       route_scale: float = 2.826, renorm_eps: float = 0.0, topk_idx=None):
+    """The layer with W8A8 experts.  `experts` = (gate, up, down), each a
+    (codes [E, rows, cols], scales [E, rows]) pair from quantize_rows_e4m3;
+    `shared` likewise for the shared expert (or None).  Routing as in
+    layer_forward (fp32 router, unquantised); each token's hidden row is
+    quantised once and read through the route index by every expert it visits."""
+    E = np.asarray(router_w).shape[0]
+    logits = router_logits(hidden, router_w)
+    if score_mode == "sigmoid":
+        r = route_sigmoid(logits, bias, top_k, route_scale)
+    elif score_mode == "softmax":
+        r = route_softmax(logits, top_k, renorm_eps)
+    else:
+        raise ValueError(score_mode)
+    idx, w = r["idx"], r["w"]
+    if topk_idx is not None:
+        idx = np.asarray(topk_idx, dtype=np.int32)
+        w = routing_weights_for(r["scores"], idx, score_mode, route_scale, renorm_eps)
+    counts, offsets = histogram_offsets(idx, E)
+    perm, inv = permutation(idx, E)
+    hq, hs = quantize_rows_e4m3(hidden)
+    (gq, gs), (uq, us), (dq, ds) = experts
+    tok = np.asarray(perm, dtype=np.int64) // top_k
+    y = np.zeros((tok.size, np.asarray(hidden).shape[1]), dtype=np.float64)
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            t = tok[lo:hi]
+            y[lo:hi] = swiglu_w8a8(hq[t], hs[t], (gq[e], gs[e]), (uq[e], us[e]), (dq[e], ds[e]))
+    z = swiglu_w8a8(hq, hs, *shared) if shared is not None else None
+    out = combine(y, inv, w, z)
+    return {"idx": idx, "w": w, "margin": r["margin"], "keys": r["keys"], "perm": perm, "inv": inv,
+            "offsets": offsets, "y_sorted": y, "z": z, "out": out}
+
+
+# ---------------------------------------------------------------------------
 # whole layer
 # ---------------------------------------------------------------------------
 
