@@ -35,7 +35,8 @@ SCORE_SIGMOID_BIAS, SCORE_SOFTMAX = 0, 1
 EXPORTS = ("moe_status_string", "moe_check_dims", "moe_workspace_bytes", "moe_ws_init", "moe_ws_read_error",
            "moe_route", "moe_permute", "moe_expert_ffn", "moe_expert_gate_up", "moe_expert_down", "moe_combine",
            "moe_layer_forward", "moe_fused_moe", "moe_expert_ffn_noalloc", "moe_selftest_wait_timeout",
-           "moe_selftest_silu", "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_layer_forward_fp8")
+           "moe_selftest_silu", "moe_quantize_fp8_rows", "moe_expert_ffn_fp8", "moe_layer_forward_fp8",
+           "moe_expert_ffn_w8a8", "moe_layer_forward_w8a8")
 
 
 class MoeError(RuntimeError):
@@ -95,6 +96,8 @@ def load() -> ctypes.CDLL:
         "moe_quantize_fp8_rows": (st, [P, ctypes.c_int64, ctypes.c_int, P, P, P]),
         "moe_expert_ffn_fp8": (st, [D, P, P, P, ctypes.POINTER(MoeFp8Experts), P, P, P, C, P]),
         "moe_layer_forward_fp8": (st, [D, P, P, P, ctypes.POINTER(MoeFp8Experts), P, P, C, P]),
+        "moe_expert_ffn_w8a8": (st, [D, P, P, P, ctypes.POINTER(MoeFp8Experts), P, P, P, C, P]),
+        "moe_layer_forward_w8a8": (st, [D, P, P, P, ctypes.POINTER(MoeFp8Experts), P, P, C, P]),
         "moe_selftest_wait_timeout": (st, [P, C, ctypes.c_ulonglong, P]),
         "moe_selftest_silu": (st, [P, P, P, ctypes.c_int64, P]),
     }
@@ -359,6 +362,34 @@ def moe_layer_forward_fp8(d: MoeDims, hidden, router_w, expert_bias, w: Fp8Exper
     _check(out, torch.bfloat16, (d.T, d.H), "out")
     _check(w.t["gate"][0], torch.uint8, (d.E, d.I, d.H), "gate codes")
     _call("moe_layer_forward_fp8", ctypes.byref(d), _ptr(hidden), _ptr(router_w), _ptr(expert_bias),
+          ctypes.byref(w.struct), _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def moe_expert_ffn_w8a8(d: MoeDims, hidden, perm, offsets, w: Fp8Experts, y_sorted, y_shared, ws,
+                        stream=None) -> None:
+    """W8A8 expert FFN: FP8 weights and FP8 activations (hidden per token, the
+    SiLU*up activation per routed slot) on the 8-bit tensor-core path."""
+    S = d.T * d.top_k
+    _check(hidden, torch.bfloat16, (d.T, d.H), "hidden")
+    _check(perm, torch.int32, (S,), "perm")
+    _check(offsets, torch.int32, (d.E + 1,), "offsets")
+    _check(y_sorted, torch.bfloat16, (S, d.H), "y_sorted")
+    _check(w.t["gate"][0], torch.uint8, (d.E, d.I, d.H), "gate codes")
+    _check(w.t["down"][0], torch.uint8, (d.E, d.H, d.I), "down codes")
+    if d.has_shared:
+        _check(y_shared, torch.bfloat16, (d.T, d.H), "y_shared")
+        _check(w.t["s_gate"][0], torch.uint8, (d.I_shared, d.H), "shared gate codes")
+    _call("moe_expert_ffn_w8a8", ctypes.byref(d), _ptr(hidden), _ptr(perm), _ptr(offsets), ctypes.byref(w.struct),
+          _ptr(y_sorted), _ptr(y_shared), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def moe_layer_forward_w8a8(d: MoeDims, hidden, router_w, expert_bias, w: Fp8Experts, out, ws, stream=None) -> None:
+    _check(hidden, torch.bfloat16, (d.T, d.H), "hidden")
+    _check(router_w, torch.float32, (d.E, d.H), "router_w")
+    _check(expert_bias, torch.float32, (d.E,), "expert_bias")
+    _check(out, torch.bfloat16, (d.T, d.H), "out")
+    _check(w.t["gate"][0], torch.uint8, (d.E, d.I, d.H), "gate codes")
+    _call("moe_layer_forward_w8a8", ctypes.byref(d), _ptr(hidden), _ptr(router_w), _ptr(expert_bias),
           ctypes.byref(w.struct), _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
 
 

@@ -123,6 +123,20 @@ bool map_u8_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, ui
   const uint32_t box[3] = {64, box_rows, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
+// E4M3 codes for the W8A8 kernel: boxes of 128 codes x box_rows, 128-byte
+// swizzle (one 128-byte K-step row per matrix row, as the bf16 maps)
+bool map_u8_2d_sw(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t str[1] = {cols};
+  const uint32_t box[2] = {128, box_rows};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+bool map_u8_3d_sw(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t n, uint32_t box_rows) {
+  const uint64_t dims[3] = {cols, rows, n};
+  const uint64_t str[2] = {cols, cols * rows};
+  const uint32_t box[3] = {128, box_rows, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, ptr, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
 // stacked bf16 [n][rows][cols] (consecutive matrices `stride_rows` rows apart,
 // rows by default), box {64, box_rows, 1}, 128-byte swizzle
 bool map_bf16_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t n, uint32_t box_rows,
@@ -140,7 +154,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
   size_t err, topk_idx, topk_w, counts, offsets, perm, inv, perm_part, y_sorted, y_shared, a_act, a_shared, w_hi,
-      w_lo, partial, total;
+      w_lo, partial, hq, hs, amax, amax_s, total;
 };
 
 // Split of H across router CTAs: a power of two <= 32 dividing H/64, with
@@ -179,6 +193,11 @@ WsLayout ws_layout(const moe_dims &d) {
   L.w_hi = take(E * (size_t)d.H * 2);
   L.w_lo = take(E * (size_t)d.H * 2);
   L.partial = take((size_t)router_ksplit(d, 256) * T * E * 4);
+  // W8A8: the hidden state's E4M3 codes and scales, and the activations' row maxima per 32 columns
+  L.hq = take(T * (size_t)d.H);
+  L.hs = take(T * 4);
+  L.amax = take(S * (size_t)(d.I / 32) * 4);
+  L.amax_s = take(T * (size_t)(Is / 32) * 4);
   L.total = off;
   return L;
 }
@@ -263,12 +282,22 @@ moe_status do_permute(const moe_dims &d, const int32_t *topk_idx, int32_t *count
 struct ExpertScratch {
   unsigned *hdr;
   __nv_bfloat16 *act, *act_s;
+  uint8_t *hq = nullptr;  // W8A8 only: the quantised hidden state and the activations' row maxima
+  float *hs = nullptr, *amax = nullptr, *amax_s = nullptr;
 };
 
 // the scratch inside a caller's workspace (moe_workspace_bytes layout)
 ExpertScratch scratch_in(const moe_dims &d, void *ws) {
   const WsLayout L = ws_layout(d);
-  return {at<unsigned>(ws, L.err), at<__nv_bfloat16>(ws, L.a_act), at<__nv_bfloat16>(ws, L.a_shared)};
+  ExpertScratch sc;
+  sc.hdr = at<unsigned>(ws, L.err);
+  sc.act = at<__nv_bfloat16>(ws, L.a_act);
+  sc.act_s = at<__nv_bfloat16>(ws, L.a_shared);
+  sc.hq = at<uint8_t>(ws, L.hq);
+  sc.hs = at<float>(ws, L.hs);
+  sc.amax = at<float>(ws, L.amax);
+  sc.amax_s = at<float>(ws, L.amax_s);
+  return sc;
 }
 
 // Tensor maps and pointers of the grouped expert FFN; `phases` selects gate/up
@@ -280,7 +309,17 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
                             const moe_bf16 *w_down, const moe_bf16 *ws_gate, const moe_bf16 *ws_up,
                             const moe_bf16 *ws_down, moe_bf16 *y_sorted, moe_bf16 *y_shared,
                             const ExpertScratch &sc, cudaStream_t stream, bool pdl, uint64_t gu_stride = 0,
-                            const moe_fp8_experts *q = nullptr) {
+                            const moe_fp8_experts *q = nullptr, bool early = false, bool w8a8 = false) {
+  // tiles of one launch at the narrowest chunking (16 tokens), for the 32-bit
+  // claim counter and tile numbers
+  {
+    const long long S = (long long)d.T * d.top_k, Is = d.has_shared ? d.I_shared : 0;
+    const long long rd = (d.H + 255) / 256;
+    const long long worst = (S / 16 + d.E + 1) * ((d.I + 127) / 128 + rd) +
+                            (d.has_shared ? (d.T / 16 + 1) * ((Is + 127) / 128 + rd) : 0);
+    if (worst >= (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+  }
+  const int bn = gemm_tile_n(d.T, d.top_k, d.E);
   GemmParams g;
   std::memset(&g, 0, sizeof(g));
   g.T = d.T;
@@ -292,6 +331,11 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
   g.S = d.T * d.top_k;
   g.has_shared = d.has_shared;
   g.phases = phases;
+  g.early = early && phases == 3 ? 1 : 0;
+  // level-major gate/up order for batches whose experts average at most 256
+  // tokens (weight streaming and MMAs overlap across SMs); segment-major for
+  // the widest tiles (token rows stay hot in L2 across an expert's row blocks)
+  g.gu_order = bn == 256 ? 0 : 1;
   g.hidden = reinterpret_cast<const __nv_bfloat16 *>(hidden);
   g.perm = perm;
   g.offsets = offsets;
@@ -302,8 +346,28 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
   g.y = reinterpret_cast<__nv_bfloat16 *>(y_sorted);
   g.y_s = reinterpret_cast<__nv_bfloat16 *>(y_shared);
   bool ok = true;
+  if (q != nullptr && w8a8) {  // W8A8: swizzled code maps, the quantised hidden state, the row maxima
+    g.mode = 2;
+    g.sc_g = q->gate_scale;
+    g.sc_u = q->up_scale;
+    g.sc_d = q->down_scale;
+    g.sc_sg = q->s_gate_scale;
+    g.sc_su = q->s_up_scale;
+    g.sc_sd = q->s_down_scale;
+    g.hq = sc.hq;
+    g.hs = sc.hs;
+    g.amax = sc.amax;
+    g.amax_s = sc.amax_s;
+    ok = map_u8_3d_sw(&g.map_wg, q->gate, d.H, d.I, d.E, 128) && map_u8_3d_sw(&g.map_wu, q->up, d.H, d.I, d.E, 128) &&
+         map_u8_3d_sw(&g.map_wd, q->down, d.I, d.H, d.E, 128);
+    if (d.has_shared)
+      ok = ok && map_u8_2d_sw(&g.map_sg, q->s_gate, d.H, g.Is, 128) &&
+           map_u8_2d_sw(&g.map_su, q->s_up, d.H, g.Is, 128) && map_u8_2d_sw(&g.map_sd, q->s_down, g.Is, d.H, 128);
+    if (!ok) return MOE_ERR_CUDA;
+    return cuda_status(launch_expert_ffn(g, bn, num_sms(), stream, pdl));
+  }
   if (q != nullptr) {  // FP8 expert weights: maps of the codes, and the row scales
-    g.q8 = 1;
+    g.mode = 1;
     g.sc_g = q->gate_scale;
     g.sc_u = q->up_scale;
     g.sc_d = q->down_scale;
@@ -319,7 +383,7 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
     if (d.has_shared)
       for (int b = 0; b < 4; ++b) ok = ok && map_bf16_2d(&g.map_acts[b], g.act_s, g.Is, d.T, 16u << b);
     if (!ok) return MOE_ERR_CUDA;
-    return cuda_status(launch_expert_ffn(g, gemm_tile_n(d.T, d.top_k, d.E), num_sms(), stream, pdl));
+    return cuda_status(launch_expert_ffn(g, bn, num_sms(), stream, pdl));
   }
   if (phases & 1) {
     ok = ok && map_bf16_3d(&g.map_wg, w_gate, d.H, d.I, d.E, 128, gu_stride) &&
@@ -336,7 +400,7 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
     }
   }
   if (!ok) return MOE_ERR_CUDA;
-  return cuda_status(launch_expert_ffn(g, gemm_tile_n(d.T, d.top_k, d.E), num_sms(), stream, pdl));
+  return cuda_status(launch_expert_ffn(g, bn, num_sms(), stream, pdl));
 }
 
 // a5-a6: gate/up GEMM through the route index + SiLU(gate) * up -> activations in ws
@@ -358,9 +422,9 @@ moe_status do_down(const moe_dims &d, const int32_t *offsets, const moe_bf16 *w_
 moe_status do_expert_ffn(const moe_dims &d, const moe_bf16 *hidden, const int32_t *perm, const int32_t *offsets,
                          const moe_bf16 *w_gate, const moe_bf16 *w_up, const moe_bf16 *w_down,
                          const moe_bf16 *ws_gate, const moe_bf16 *ws_up, const moe_bf16 *ws_down, moe_bf16 *y_sorted,
-                         moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl) {
+                         moe_bf16 *y_shared, void *ws, cudaStream_t stream, bool pdl, bool early = false) {
   return do_expert_phases(d, 3, hidden, perm, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_sorted,
-                          y_shared, scratch_in(d, ws), stream, pdl);
+                          y_shared, scratch_in(d, ws), stream, pdl, 0, nullptr, early);
 }
 
 moe_status do_combine(const moe_dims &d, const moe_bf16 *y_sorted, const moe_bf16 *y_shared, const int32_t *inv,
@@ -404,7 +468,7 @@ moe_status do_fused_moe(const moe_dims &d, const moe_bf16 *hidden, const int32_t
   const size_t up = (size_t)d.I * d.H, sup = d.has_shared ? (size_t)d.I_shared * d.H : 0;
   st = do_expert_phases(d, 3, hidden, perm, offs, w_gate_up, w_gate_up + up, w_down, ws_gate_up,
                         d.has_shared ? ws_gate_up + sup : nullptr, ws_down, y, z, scratch_in(d, ws), s, true,
-                        2 * (uint64_t)d.I);
+                        2 * (uint64_t)d.I, nullptr, true);
   if (st != MOE_OK) return st;
   return do_combine(d, y, z, inv, topk_w, out, s, true);
 }
@@ -621,7 +685,63 @@ MOE_API moe_status moe_layer_forward_fp8(const moe_dims *d, const moe_bf16 *hidd
   if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, wt, ws, s, true)) != MOE_OK) return st;
   if ((st = do_permute(*d, idx, at<int32_t>(ws, L.counts), offs, perm, inv, ws, s, true)) != MOE_OK) return st;
   if ((st = do_expert_phases(*d, 3, hidden, perm, offs, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, y, z,
-                             scratch_in(*d, ws), s, true, 0, w)) != MOE_OK)
+                             scratch_in(*d, ws), s, true, 0, w, true)) != MOE_OK)
+    return st;
+  return do_combine(*d, y, z, inv, wt, out, s, true);
+}
+
+// W8A8 needs 128-element K steps: H, I and I_shared multiples of 128.
+bool w8a8_shape_ok(const moe_dims &d) {
+  return d.H % 128 == 0 && d.I % 128 == 0 && (!d.has_shared || d.I_shared % 128 == 0);
+}
+
+MOE_API moe_status moe_expert_ffn_w8a8(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
+                                       const int32_t *offsets, const moe_fp8_experts *w, moe_bf16 *y_sorted,
+                                       moe_bf16 *y_shared, void *ws, size_t ws_bytes, void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (!w8a8_shape_ok(*d)) return MOE_ERR_UNSUPPORTED;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(hidden) || !ptr_ok(perm) || !ptr_ok(offsets) || !ptr_ok(y_sorted) || !fp8_ok(*d, w))
+    return MOE_ERR_INVALID_ARG;
+  if (d->has_shared && !ptr_ok(y_shared)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const ExpertScratch sc = scratch_in(*d, ws);
+  if (launch_quantize_rows(reinterpret_cast<const __nv_bfloat16 *>(hidden), sc.hq, sc.hs, d->T, d->H, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return do_expert_phases(*d, 3, hidden, perm, offsets, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                          y_sorted, y_shared, sc, s, true, 0, w, false, true);
+}
+
+MOE_API moe_status moe_layer_forward_w8a8(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
+                                          const float *expert_bias, const moe_fp8_experts *w, moe_bf16 *out,
+                                          void *ws, size_t ws_bytes, void *stream) {
+  moe_status st = moe_check_dims(d);
+  if (st != MOE_OK) return st;
+  if (!w8a8_shape_ok(*d)) return MOE_ERR_UNSUPPORTED;
+  if (d->T == 0) return MOE_OK;
+  if (!ptr_ok(hidden) || !ptr_ok(router_w) || !ptr_ok(out) || !fp8_ok(*d, w)) return MOE_ERR_INVALID_ARG;
+  if (expert_bias != nullptr && !aligned16(expert_bias)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != MOE_OK) return st;
+  const WsLayout L = ws_layout(*d);
+  cudaStream_t s = (cudaStream_t)stream;
+  const ExpertScratch sc = scratch_in(*d, ws);
+  int32_t *idx = at<int32_t>(ws, L.topk_idx);
+  float *wt = at<float>(ws, L.topk_w);
+  int32_t *perm = at<int32_t>(ws, L.perm), *inv = at<int32_t>(ws, L.inv);
+  int32_t *offs = at<int32_t>(ws, L.offsets);
+  moe_bf16 *y = at<moe_bf16>(ws, L.y_sorted), *z = at<moe_bf16>(ws, L.y_shared);
+  // the hidden state is quantised first, so that it is complete before the
+  // expert kernel's early (routing-independent) tiles read it
+  if (launch_quantize_rows(reinterpret_cast<const __nv_bfloat16 *>(hidden), sc.hq, sc.hs, d->T, d->H, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, wt, ws, s, true)) != MOE_OK) return st;
+  if ((st = do_permute(*d, idx, at<int32_t>(ws, L.counts), offs, perm, inv, ws, s, true)) != MOE_OK) return st;
+  if ((st = do_expert_phases(*d, 3, hidden, perm, offs, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, y, z,
+                             sc, s, true, 0, w, true, true)) != MOE_OK)
     return st;
   return do_combine(*d, y, z, inv, wt, out, s, true);
 }
@@ -649,7 +769,7 @@ MOE_API moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, 
   if ((st = do_route(*d, hidden, router_w, expert_bias, nullptr, idx, w, ws, s, true)) != MOE_OK) return st;
   if ((st = do_permute(*d, idx, at<int32_t>(ws, L.counts), offs, perm, inv, ws, s, true)) != MOE_OK) return st;
   if ((st = do_expert_ffn(*d, hidden, perm, offs, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y, z, ws, s,
-                          true)) != MOE_OK)
+                          true, true)) != MOE_OK)
     return st;
   return do_combine(*d, y, z, inv, w, out, s, true);
 }

@@ -27,14 +27,17 @@
 // far below the rate these tiles need); the activation rows of a down tile,
 // which are contiguous, by at most four TMA boxes.
 //
-// Scheduling.  The tile list is every gate/up tile (per segment: 128-row
-// blocks of I x token chunks, chunks innermost so they reuse the block's
-// weights in L2) followed by every down tile.  CTAs (one per SM) claim tiles
-// in that order from an atomic counter, so a down tile is claimed only after
-// every gate/up tile has been claimed by a running CTA: its wait for the
-// gate/up tiles of its segment (a per-segment completion count, bounded) can
-// always be satisfied, whatever the residency of other CTAs.  Gate/up tiles
-// never wait.  The last CTA to leave zeroes the counters for the next call.
+// Scheduling.  CTAs (one per SM) claim tiles from an atomic counter in a fixed
+// order (see "Claim order" below): an early block of shared-expert gate/up
+// tiles, the remaining gate/up tiles, then every down tile.  A down tile is
+// thus claimed only after every gate/up tile has been claimed by a running
+// CTA: its wait for the gate/up tiles of its segment (a per-segment completion
+// count, bounded) can always be satisfied, whatever the residency of other
+// CTAs.  Gate/up tiles never wait.  In the layer chain the early block needs
+// no routing, so it runs while the router and the permutation still do
+// (programmatic dependent launch: the routing kernels let this one launch as
+// soon as they start).  The last CTA to leave zeroes the counters for the next
+// call.
 //
 // Pipelines.  Weights stream from HBM and need the longer lead; token rows
 // come from L2.  So the two operands have rings of their own: kW weight slots
@@ -45,7 +48,8 @@
 // token tiles four, 256-token tiles three (fewer than three token slots
 // starve the MMA).
 //
-// Warp roles: 0 (one thread) claims tiles and issues the weight TMA loads; 1-4
+// Warp roles: 0 claims tiles and issues the weight TMA loads (lane 0) and
+// builds the claim-order tables once the routing is visible (whole warp); 1-4
 // load token rows (cp.async) or activation rows (TMA, one thread) and wait for
 // a down tile's gate/up tiles; 5 issues the MMAs (one thread) and owns TMEM;
 // 6-21 drain the accumulators, four warps per TMEM lane quarter taking its
@@ -55,6 +59,7 @@
 // tile's epilogue with the next tile's MMAs (BN = 256 fills TMEM with one pair).
 #include <cuda_fp8.h>
 
+#include "fp8.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "silu.cuh"
@@ -65,6 +70,13 @@ namespace {
 
 constexpr int kABytes = 2 * 128 * 128;  // weights of one K step: two 128-row x 64-bf16 boxes
 constexpr int kMaxSeg = 258;            // E <= 256 routed + 1 shared (+1 sentinel)
+// Runs of the claim order (see SchedTables): gate/up at most 2 per row-block
+// level (I <= 16384: 128 levels) + 2; down at most E + H / 256 = 256 + 64.
+constexpr int kMaxRuns = 580;
+// Shared-expert gate/up tiles claimed ahead of everything else (whole row-block
+// levels, at least one): in the layer chain they run before the routing is known.
+constexpr int kEarlyTiles = 32;
+constexpr int kGroupSegs = 32;  // routed segments per group of the level-major gate/up order
 constexpr int kWWarp = 0;               // tile claims + weight loads (lane 0)
 constexpr int kTokWarp0 = 1;            // warps 1-4: token / activation loads
 constexpr int kTokThreads = 128;
@@ -80,22 +92,28 @@ constexpr int kRing = 4;                // claimed tile ids in flight
 constexpr int kQBytes = 2 * 128 * 64;
 constexpr int kCvtWarps = 8;
 constexpr unsigned long long kDrainNs = 20000000ull;
+// Kernel modes: bf16 weights; FP8 weights expanded to bf16 in shared memory by
+// converter warps (weight-only); W8A8 -- FP8 weights and FP8 activations fed
+// straight to kind::f8f6f4 MMAs (K steps of 128 codes: 128-byte rows again).
+constexpr int kModeBF16 = 0, kModeQ8 = 1, kModeF8 = 2;
 
 // Ring depths: weight slots of 32 KB and token slots of BN x 128 bytes; with
 // FP8 weights, code slots of 16 KB (the bytes in flight from HBM) and three
 // bf16 weight slots between the converters and the MMAs.
-template <int BN, bool Q8>
+template <int BN, int MODE>
 struct Rings {
+  static constexpr bool Q8 = MODE == kModeQ8;
   static constexpr int kW = Q8 ? 3 : BN >= 256 ? 3 : BN >= 240 ? 4 : BN >= 128 ? 5 : 6;
   static constexpr int kQ = Q8 ? (BN >= 128 ? 4 : 6) : 0;
   static constexpr int kT = BN >= 64 ? 3 : 4;
 };
 
-template <int BN, bool Q8>
+template <int BN, int MODE>
 struct Layout {
-  static constexpr int kW = Rings<BN, Q8>::kW;
-  static constexpr int kQ = Rings<BN, Q8>::kQ;
-  static constexpr int kT = Rings<BN, Q8>::kT;
+  static constexpr bool Q8 = MODE == kModeQ8;
+  static constexpr int kW = Rings<BN, MODE>::kW;
+  static constexpr int kQ = Rings<BN, MODE>::kQ;
+  static constexpr int kT = Rings<BN, MODE>::kT;
   static constexpr int kEpiW = Q8 ? kEpiWarps - kCvtWarps : kEpiWarps;  // epilogue warps
   static constexpr int kTokBytes = BN * 128;
   static constexpr int kQOff = kW * kABytes;
@@ -108,11 +126,13 @@ struct Layout {
   // wfull, wempty per weight slot; tfull, tempty per token slot; acc full[2],
   // acc empty[2]; drain; id_full[kRing], id_empty[kRing]; qfull, qempty per code slot
   static constexpr int kNumBars = 2 * kW + 2 * kT + 5 + 2 * kRing + 2 * kQ;
-  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;     // tmem slot, abort flag, ring of tile ids
-  static constexpr int kStart1Off = kMiscOff + 64;
-  static constexpr int kStart2Off = kStart1Off + 4 * kMaxSeg;
-  static constexpr int kOffOff = kStart2Off + 4 * kMaxSeg;
-  static constexpr int kBytes = kOffOff + 4 * kMaxSeg;
+  // tmem slot, abort flag, ring of tile ids, schedule scalars (SchedMisc)
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+  static constexpr int kSegOffOff = kMiscOff + 128;           // routed segment offsets [E + 1]
+  static constexpr int kCstOff = kSegOffOff + 4 * kMaxSeg;    // routed chunk prefix [E + 1]
+  static constexpr int kRunStartOff = kCstOff + 4 * kMaxSeg;  // first tile of each run [runs + 1]
+  static constexpr int kRunDescOff = kRunStartOff + 4 * (kMaxRuns + 1);
+  static constexpr int kBytes = kRunDescOff + 4 * kMaxRuns;
   static constexpr size_t kSmem = 1024 + kBytes;
   // accumulator pairs of 2 x BN columns: two while they fit in 512 columns, else one
   static constexpr int kAccBufs = 4 * BN <= 512 ? 2 : 1;
@@ -124,6 +144,7 @@ struct Layout {
   static_assert(kTmemUsed <= 512, "TMEM budget");
   static_assert(kW <= 16 && kT <= 16 && kQ <= 16, "issue masks");
   static_assert(!Q8 || BN <= 128, "FP8 weights run the narrow tiles");
+  static_assert(MODE != kModeF8 || BN <= 240, "the W8A8 epilogue has no staged (256-token) form");
 };
 
 struct Tile {
@@ -146,43 +167,235 @@ __device__ __forceinline__ int chunk_count(int cnt) {
   return (cnt + b - 1) / b;
 }
 
-// Weight row blocks of a segment: 128 gate/up pairs, or 256 rows of w_down.
-__device__ __forceinline__ int seg_nrb(const GemmParams &p, int phase, bool shared) {
-  if (phase == 0) return ((shared ? p.Is : p.I) + 127) >> 7;
-  return (p.H + 255) >> 8;
-}
+// Claim order.  Tiles are numbered in the order CTAs claim them, as runs:
+//   early block  the shared expert's gate/up tiles of row blocks [0, r_e) --
+//                 they need only `hidden`, so in the layer chain they start
+//                 before the routing is known (no table needed to decode them);
+//   gate/up      grouped level-major (gu_order 1): the routed segments in groups
+//                 (about 32 each), group after group; inside a group, for each
+//                 128-row block r, a "level" run of every segment's chunks at r;
+//                 after each group, its share of the shared expert's remaining
+//                 row blocks.  In-flight tiles then mix experts of every size --
+//                 few-token tiles that stream weights from HBM and many-token
+//                 chunks whose weights are L2 hits -- so the two bounds overlap
+//                 across SMs, while a group's experts still finish early enough
+//                 for their down tiles not to wait.  Or segment-major (gu_order 0): each
+//                 routed segment's row blocks in turn (chunks innermost), then the
+//                 shared expert's remaining row blocks, which keeps one expert's
+//                 token rows hot in L2 across its row blocks (many-token batches);
+//   down         each routed segment's row blocks in turn (chunks innermost: the
+//                 activations of a chunk are re-read from L2 by its row blocks),
+//                 with the shared expert's row blocks spread evenly between
+//                 them instead of forming one long compute-bound run.
+// A run is either one segment's row blocks [rb, rb + cnt) in (row block,
+// chunk) order, or a level (all routed segments of one group at one row block).
+constexpr int kRunLevel = 1 << 30;
+__host__ __device__ constexpr int run_desc(int seg, int rb, int cnt) { return seg | (rb << 9) | (cnt << 17); }
+__device__ __forceinline__ int run_seg(int d) { return d & 0x1FF; }
+__device__ __forceinline__ int run_rb(int d) { return (d >> 9) & 0xFF; }
 
-__device__ __forceinline__ int seg_count(const GemmParams &p, const int *seg_off, int s) {
-  return s == p.E ? p.T : seg_off[s + 1] - seg_off[s];
-}
-
+// Scalars of the claim order that depend only on the dims (known before routing).
+struct Sched {
+  int nch_s;    // chunks of the shared segment (T tokens)
+  int Rr, Rs;   // gate/up row blocks of a routed / the shared expert (0 when not run)
+  int Rd;       // down row blocks (0 when not run)
+  int r_e;      // shared row blocks in the early block
+  int n_early;  // r_e * nch_s
+  int ngroups, gsize;  // grouped level-major gate/up order: groups of gsize routed segments
+};
 template <int BN>
-__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const int *start1, const int *start2,
-                                            const int *seg_off, int nseg) {
+__device__ __forceinline__ Sched make_sched(const GemmParams &p) {
+  Sched q;
+  const bool gu = p.phases & 1, dn = p.phases & 2, sh = p.has_shared != 0;
+  q.nch_s = sh ? chunk_count<BN>(p.T) : 0;
+  q.Rr = gu ? (p.I + 127) >> 7 : 0;
+  q.Rs = (gu && sh) ? (p.Is + 127) >> 7 : 0;
+  q.Rd = dn ? (p.H + 255) >> 8 : 0;
+  q.r_e = q.Rs > 0 ? max(1, min(q.Rs, kEarlyTiles / q.nch_s)) : 0;
+  q.n_early = q.r_e * q.nch_s;
+  // groups of about kGroupSegs segments, few enough that their level runs fit
+  // the run table (at most 256 + 8 gate/up runs)
+  q.ngroups = max(1, min((p.E + kGroupSegs - 1) / kGroupSegs, 256 / (q.Rr + 1)));
+  q.gsize = (p.E + q.ngroups - 1) / q.ngroups;
+  return q;
+}
+
+// Tables written once per CTA (by warp 0, after the routing is visible) and
+// read by every role: schedule totals in shared memory.
+struct SchedMisc {
+  int total;      // tiles of both phases
+  int n_gu_runs;  // runs [0, n_gu_runs) are gate/up, the rest down
+  int n_runs;
+};
+
+template <int BN, int KSH>
+__device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const Sched &q, const SchedMisc &m,
+                                            const int *seg_off, const int *cst, const int *rstart, const int *rdesc) {
   Tile tl;
-  tl.phase = t < start1[nseg] ? 0 : 1;
-  const int *ts = tl.phase == 0 ? start1 : start2;
-  const int u = tl.phase == 0 ? t : t - start1[nseg];
-  int lo = 0, hi = nseg;  // ts[nseg] = total of the phase > u
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (ts[mid] <= u) lo = mid;
-    else hi = mid;
+  int seg, rb, ch;
+  if (t < q.n_early) {
+    tl.phase = 0;
+    seg = p.E;
+    rb = t / q.nch_s;
+    ch = t - rb * q.nch_s;
+  } else {
+    int lo = 0, hi = m.n_runs;  // the last run starting at or before t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (rstart[mid] <= t) lo = mid;
+      else hi = mid;
+    }
+    tl.phase = lo < m.n_gu_runs ? 0 : 1;
+    const int d = rdesc[lo];
+    const int local = t - rstart[lo];
+    if (d & kRunLevel) {
+      rb = run_rb(d);
+      const int s_lo = run_seg(d) * q.gsize;  // the group's segments [s_lo, s_hi)
+      const int key = local + cst[s_lo];
+      int a = s_lo, b = min(p.E, s_lo + q.gsize);  // the last segment whose chunks start at or before key
+      while (b - a > 1) {
+        const int mid = (a + b) >> 1;
+        if (cst[mid] <= key) a = mid;
+        else b = mid;
+      }
+      seg = a;
+      ch = key - cst[a];
+    } else {
+      seg = run_seg(d);
+      const int nch = seg == p.E ? q.nch_s : cst[seg + 1] - cst[seg];
+      const int qq = local / nch;
+      rb = run_rb(d) + qq;
+      ch = local - qq * nch;
+    }
   }
-  tl.seg = lo;
-  tl.shared = (lo == p.E) ? 1 : 0;
-  const int cnt = seg_count(p, seg_off, lo);
-  const int nch = chunk_count<BN>(cnt);
-  const int local = u - ts[lo];
-  tl.rb = local / nch;
-  const int ch = local - tl.rb * nch;
+  tl.seg = seg;
+  tl.shared = seg == p.E ? 1 : 0;
+  tl.rb = rb;
+  const int cnt = tl.shared ? p.T : seg_off[seg + 1] - seg_off[seg];
   const int base = chunk_base<BN>(cnt);
   const int pin = ch * base;
   tl.ntok = min(base, cnt - pin);
-  tl.row0 = (tl.shared ? 0 : seg_off[lo]) + pin;
+  tl.row0 = (tl.shared ? 0 : seg_off[seg]) + pin;
   tl.N = (tl.ntok + 15) & ~15;
-  tl.nk = tl.phase == 0 ? (p.H >> 6) : ((tl.shared ? p.Is : p.I) >> 6);
+  tl.nk = tl.phase == 0 ? (p.H >> KSH) : ((tl.shared ? p.Is : p.I) >> KSH);  // K steps of 2^KSH
   return tl;
+}
+
+// Warp 0 builds the run tables once the routing (offsets) is visible.  Every
+// lane fills its own entries; no entry depends on another lane's but through
+// the chunk prefix, which the warp scans first.
+template <int BN>
+__device__ void build_sched_tables(const GemmParams &p, const Sched &q, SchedMisc *m, int *seg_off, int *cst,
+                                   int *rstart, int *rdesc, int lane) {
+  const int E = p.E;
+  for (int i = lane; i <= E; i += 32) seg_off[i] = __ldg(p.offsets + i);
+  __syncwarp();
+  bool good = true;
+  for (int i = lane; i <= E; i += 32) {
+    if (i == 0) good = good && seg_off[0] == 0;
+    else good = good && seg_off[i] >= seg_off[i - 1];
+    if (i == E) good = good && seg_off[i] == p.S;
+  }
+  good = __all_sync(0xffffffffu, good);
+  if (!good && blockIdx.x == 0 && lane == 0 && p.err != nullptr) atomicOr(p.err, MOE_DEVERR_OFFSETS);
+  // routed chunk prefix (no routed work at all when the offsets are bad)
+  const int per = (E + 31) / 32, s0 = lane * per, s1 = min(E, s0 + per);
+  int local = 0;
+  for (int s = s0; s < s1; ++s) local += good ? chunk_count<BN>(seg_off[s + 1] - seg_off[s]) : 0;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - local;
+  for (int s = s0; s < s1; ++s) {
+    cst[s] = run;
+    run += good ? chunk_count<BN>(seg_off[s + 1] - seg_off[s]) : 0;
+  }
+  if (lane == 31) cst[E] = incl;
+  __syncwarp();
+  const int C = cst[E];
+  // ---- gate/up runs
+  const int base = q.Rs > 0 ? 1 : 0;  // run 0: the early block
+  if (lane == 0 && base) {
+    rstart[0] = 0;
+    rdesc[0] = run_desc(E, 0, q.r_e);
+  }
+  int n_gu = base, G1 = q.n_early;
+  if (p.gu_order == 1 && q.Rr > 0) {  // grouped level-major
+    // lane g < ngroups: group g's level runs, then its share of the shared
+    // expert's remaining row blocks; run and tile offsets by a scan over groups
+    const int g = lane;
+    const bool has = g < q.ngroups;
+    const int s_lo = has ? min(E, g * q.gsize) : E, s_hi = has ? min(E, s_lo + q.gsize) : E;
+    const int Cg = cst[s_hi] - cst[s_lo];
+    const int rrem = max(0, q.Rs - q.r_e);
+    const int lo_g = has ? g * rrem / q.ngroups : 0, hi_g = has ? (g + 1) * rrem / q.ngroups : 0;
+    const int my_tiles = has ? q.Rr * Cg + (hi_g - lo_g) * q.nch_s : 0;
+    const int my_runs = has ? q.Rr + (hi_g > lo_g ? 1 : 0) : 0;
+    int t_incl = my_tiles, r_incl = my_runs;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, t_incl, o), b = __shfl_up_sync(0xffffffffu, r_incl, o);
+      if (lane >= o) {
+        t_incl += a;
+        r_incl += b;
+      }
+    }
+    if (has) {
+      int idx = base + r_incl - my_runs;
+      const int st = q.n_early + t_incl - my_tiles;
+      for (int r = 0; r < q.Rr; ++r, ++idx) {
+        rstart[idx] = st + r * Cg;
+        rdesc[idx] = kRunLevel | run_desc(g, r, 0);
+      }
+      if (hi_g > lo_g) {
+        rstart[idx] = st + q.Rr * Cg;
+        rdesc[idx] = run_desc(E, q.r_e + lo_g, hi_g - lo_g);
+      }
+    }
+    n_gu += __shfl_sync(0xffffffffu, r_incl, 31);
+  } else if (q.Rr > 0) {  // segment-major
+    for (int s = lane; s < E; s += 32) {
+      rstart[base + s] = q.n_early + q.Rr * cst[s];
+      rdesc[base + s] = run_desc(s, 0, q.Rr);
+    }
+    n_gu += E;
+    if (q.Rs > q.r_e) {
+      if (lane == 0) {
+        rstart[n_gu] = q.n_early + q.Rr * C;
+        rdesc[n_gu] = run_desc(E, q.r_e, q.Rs - q.r_e);
+      }
+      ++n_gu;
+    }
+  }
+  G1 += q.Rr * C + max(0, q.Rs - q.r_e) * q.nch_s;
+  // ---- down runs: routed segments, shared row blocks spread between them
+  int n_runs = n_gu, total = G1;
+  if (q.Rd > 0) {
+    const int nsd = p.has_shared ? q.Rd : 0;
+    for (int s = lane; s < E; s += 32) {
+      const int nsh = min(nsd, (s * nsd) / E);  // shared row blocks placed before routed segment s
+      rstart[n_gu + s + nsh] = G1 + q.Rd * cst[s] + nsh * q.nch_s;
+      rdesc[n_gu + s + nsh] = run_desc(s, 0, q.Rd);
+    }
+    for (int dd = lane; dd < nsd; dd += 32) {
+      const int sd = ((dd + 1) * E + nsd - 1) / nsd - 1;  // placed after routed segment sd
+      rstart[n_gu + sd + 1 + dd] = G1 + q.Rd * cst[sd + 1] + dd * q.nch_s;
+      rdesc[n_gu + sd + 1 + dd] = run_desc(E, dd, 1);
+    }
+    n_runs += E + nsd;
+    total += q.Rd * C + nsd * q.nch_s;
+  }
+  if (lane == 0) {
+    rstart[n_runs] = total;
+    m->total = total;
+    m->n_gu_runs = n_gu;
+    m->n_runs = n_runs;
+  }
+  __threadfence_block();  // every lane's entries before lane 0 releases them (id_full)
+  __syncwarp();
 }
 
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -211,6 +424,25 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Column maxima of a warp's 32 rows x 16 columns: m[j] is this lane's value of
+// column j.  Four halving exchanges (8 + 4 + 2 + 1 shuffles) and a last pair
+// leave in m[0] the maximum over all 32 lanes of the column returned, which
+// lanes 2c and 2c + 1 share for c = 0..15.
+__device__ __forceinline__ int col_max16(float (&m)[16], int lane) {
+#pragma unroll
+  for (int half = 8, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+    const bool upper = lane & bit;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = upper ? m[k] : m[half + k];
+      const float keep = upper ? m[half + k] : m[k];
+      m[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, bit));
+    }
+  }
+  m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
 // Eight E4M3 codes (two little-endian words, first code in the low byte) to the
 // eight bf16 values they encode, exactly (every E4M3 value is a bf16 value; the
 // row scale is applied to the fp32 accumulators in the epilogue instead).
@@ -229,9 +461,12 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16(uint32_t w0, uint32_t w1) {
 
 }  // namespace
 
-template <int BN, bool Q8>
+template <int BN, int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __grid_constant__ GemmParams p) {
-  using L = Layout<BN, Q8>;
+  using L = Layout<BN, MODE>;
+  constexpr bool Q8 = MODE == kModeQ8, F8 = MODE == kModeF8;
+  constexpr int KE = F8 ? 128 : 64;  // K elements per step: one 128-byte row of a weight or token box
+  constexpr int KSH = F8 ? 7 : 6;
   constexpr int KW = L::kW, KT = L::kT, KQ = L::kQ, EW = L::kEpiW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -239,9 +474,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   uint32_t *tmem_slot = (uint32_t *)(smem + L::kMiscOff);
   volatile int *abort_flag = (volatile int *)(smem + L::kMiscOff + 4);
   volatile int *ring = (volatile int *)(smem + L::kMiscOff + 16);  // kRing claimed tile ids
-  int *start1 = (int *)(smem + L::kStart1Off);
-  int *start2 = (int *)(smem + L::kStart2Off);
-  int *seg_off = (int *)(smem + L::kOffOff);
+  SchedMisc *misc = (SchedMisc *)(smem + L::kMiscOff + 32);
+  int *seg_off = (int *)(smem + L::kSegOffOff);
+  int *cst = (int *)(smem + L::kCstOff);
+  int *rstart = (int *)(smem + L::kRunStartOff);
+  int *rdesc = (int *)(smem + L::kRunDescOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto wfull_bar = [&](int s) { return smem_u32(&bars[s]); };
@@ -300,77 +537,75 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  pdl_wait();  // perm / offsets / activations come from the previous kernel
+  // Dependents may launch now: every kernel of this library waits for its
+  // predecessor's completion before it reads what that one wrote.
   pdl_launch_dependents();
-
-  // ---------------- tile lists of both phases from the expert offsets (one warp)
-  const int nseg = p.E + (p.has_shared ? 1 : 0);
-  if (warp == kMmaWarp) {
-    for (int i = lane; i <= p.E; i += 32) seg_off[i] = __ldg(p.offsets + i);
-    __syncwarp();
-    bool good = true;
-    for (int i = lane; i <= p.E; i += 32) {
-      if (i == 0) good = good && seg_off[0] == 0;
-      else good = good && seg_off[i] >= seg_off[i - 1];
-      if (i == p.E) good = good && seg_off[i] == p.S;
-    }
-    good = __all_sync(0xffffffffu, good);
-    if (!good && blockIdx.x == 0 && lane == 0 && p.err != nullptr) atomicOr(p.err, MOE_DEVERR_OFFSETS);
-    const int per = (nseg + 31) / 32;
-    const int s0 = lane * per;
-#pragma unroll
-    for (int ph = 0; ph < 2; ++ph) {
-      int *ts = ph == 0 ? start1 : start2;
-      const bool on = good && (p.phases >> ph) & 1;
-      int local = 0;
-      for (int s = s0; s < min(nseg, s0 + per); ++s)
-        local += on ? chunk_count<BN>(seg_count(p, seg_off, s)) * seg_nrb(p, ph, s == p.E) : 0;
-      int incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
+  // Routing data (perm, offsets) comes from the previous kernel.  With p.early
+  // the early block's tiles (the shared expert's first row blocks) proceed
+  // before it is visible, and each role waits only when it first meets a tile
+  // that needs it; otherwise every thread waits here.
+  if (!p.early) pdl_wait();
+  const Sched q = make_sched<BN>(p);
+  if (p.early && q.Rs > 0 && warp == kWWarp && lane == 0) {
+    // The shared expert's weights into L2 while the routing still runs: none
+    // of its tiles depends on the routing, and the early block alone would
+    // stream them from a few SMs.  Each CTA takes a strided share of the
+    // 64 x 128 boxes of ws_gate, ws_up and ws_down.
+    const int kx_gu = p.H / KE, n_gu = kx_gu * ((p.Is + 127) / 128);
+    const int kx_d = p.Is / KE, n_d = kx_d * ((p.H + 127) / 128);
+    for (int b = blockIdx.x; b < 2 * n_gu + n_d; b += gridDim.x) {
+      if (b < 2 * n_gu) {
+        const int bb = b < n_gu ? b : b - n_gu;
+        tma_prefetch_l2_2d(b < n_gu ? &p.map_sg : &p.map_su, (bb % kx_gu) * KE, (bb / kx_gu) * 128);
+      } else {
+        const int bb = b - 2 * n_gu;
+        tma_prefetch_l2_2d(&p.map_sd, (bb % kx_d) * KE, (bb / kx_d) * 128);
       }
-      int run = incl - local;
-      for (int s = s0; s < min(nseg, s0 + per); ++s) {
-        ts[s] = run;
-        run += on ? chunk_count<BN>(seg_count(p, seg_off, s)) * seg_nrb(p, ph, s == p.E) : 0;
-      }
-      if (lane == 31) ts[nseg] = incl;
     }
   }
-  __syncthreads();
-  const int total = start1[nseg] + start2[nseg];
   unsigned *err = p.err;
   unsigned *claim = p.sync + kSyncClaim;
   unsigned *done1 = p.sync + kSyncDone;  // gate/up tiles finished, per segment
   bool ok = true;
+  auto decode = [&](int t) { return decode_tile<BN, KSH>(p, t, q, *misc, seg_off, cst, rstart, rdesc); };
 
   if (warp == kWWarp) {
-    // ================= tile claims and weight loads (one thread); FP8 weights
-    // go to the code slots, bf16 weights straight to the weight slots
-    if (lane == 0) {
-      constexpr int NS = Q8 ? KQ : KW;
-      const uint64_t pol_w = policy_evict_first();
-      int ws = 0;
-      uint32_t wph = 0;
-      uint32_t issued = 0, issued_par = 0;  // per weight slot: a load issued, and its phase parity
-      for (int i = 0; ok; ++i) {
-        const int r = i % kRing;
-        ok = mbar_wait(id_empty(r), ((uint32_t)(i / kRing) & 1u) ^ 1u, err, abort_flag);
-        if (!ok) break;
-        const int t0 = (int)atomicAdd(claim, 1u);
-        const int t = t0 < total ? t0 : -1;
+    // ================= tile claims and weight loads.  Lane 0 claims tiles and
+    // issues the weight TMA loads (FP8 weights to the code slots, bf16 weights
+    // straight to the weight slots); the whole warp builds the claim-order
+    // tables when the first tile past the early block is claimed.
+    constexpr int NS = Q8 ? KQ : KW;
+    const uint64_t pol_w = policy_evict_first();
+    int ws = 0;
+    uint32_t wph = 0;
+    uint32_t issued = 0, issued_par = 0;  // per weight slot: a load issued, and its phase parity
+    bool tables = false;
+    for (int i = 0; ok; ++i) {
+      const int r = i % kRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(id_empty(r), ((uint32_t)(i / kRing) & 1u) ^ 1u, err, abort_flag));
+      if (!ok) break;
+      int t0 = 0;
+      if (lane == 0) t0 = (int)atomicAdd(claim, 1u);
+      t0 = __shfl_sync(0xffffffffu, t0, 0);
+      if (t0 >= q.n_early && !tables) {
+        if (p.early) pdl_wait();
+        build_sched_tables<BN>(p, q, misc, seg_off, cst, rstart, rdesc, lane);
+        tables = true;
+      }
+      const int t = t0 < q.n_early ? t0 : (t0 < misc->total ? t0 : -1);
+      if (lane == 0) {
         ring[r] = t;
-        mbar_arrive(id_full(r));
-        if (t < 0) break;
-        const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+        mbar_arrive(id_full(r));  // release: the tables above are visible to the roles that take this id
+      }
+      if (t < 0) break;
+      if (lane == 0) {
+        const Tile tl = decode(t);
         const int i0 = tl.rb * (tl.phase == 0 ? 128 : 256);
         for (int kb = 0; kb < tl.nk; ++kb) {
           const uint32_t fb = Q8 ? qfull_bar(ws) : wfull_bar(ws);
           ok = mbar_wait(Q8 ? qempty_bar(ws) : wempty_bar(ws), wph ^ 1u, err, abort_flag);
           if (!ok) break;
-          const int k0 = kb * 64;
+          const int k0 = kb * KE;
           mbar_arrive_expect_tx(fb, (uint32_t)(Q8 ? kQBytes : kABytes));
           issued |= 1u << ws;
           issued_par = (issued_par & ~(1u << ws)) | (wph << ws);
@@ -398,10 +633,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
           }
         }
       }
-      if (!ok)
-        for (int s = 0; s < NS; ++s)
-          if ((issued >> s) & 1u) mbar_wait_drain(Q8 ? qfull_bar(s) : wfull_bar(s), (issued_par >> s) & 1u);
+      ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
     }
+    if (!ok && lane == 0)
+      for (int s2 = 0; s2 < NS; ++s2)
+        if ((issued >> s2) & 1u) mbar_wait_drain(Q8 ? qfull_bar(s2) : wfull_bar(s2), (issued_par >> s2) & 1u);
   } else if (warp < kTokWarp0 + 4) {
     // ================= token rows (gate/up) or activation rows (down)
     const int tid = threadIdx.x - 32 * kTokWarp0;  // 0..127
@@ -409,6 +645,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
     int ts = 0;
     uint32_t tph = 0;
     uint32_t issued = 0, issued_par = 0;  // per token slot: an activation TMA issued (thread 0)
+    bool waited = !p.early;
     for (int i = 0; ok; ++i) {
       const int r = i % kRing;
       ok = __all_sync(0xffffffffu, mbar_wait(id_full(r), (uint32_t)(i / kRing) & 1u, err, abort_flag));
@@ -417,11 +654,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       __syncwarp();
       if (lane == 0) mbar_arrive(id_empty(r));
       if (t < 0) break;
-      const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+      if (t >= q.n_early && !waited) {  // perm comes from the previous kernel
+        pdl_wait();
+        waited = true;
+      }
+      const Tile tl = decode(t);
 
       // ---- a down tile needs every gate/up tile of its segment
       if (tl.phase == 1 && (p.phases & 1) && tid == 0) {
-        const unsigned need = (unsigned)(chunk_count<BN>(seg_count(p, seg_off, tl.seg)) * seg_nrb(p, 0, tl.shared));
+        const int nch = tl.shared ? q.nch_s : cst[tl.seg + 1] - cst[tl.seg];
+        const unsigned need = (unsigned)(nch * (tl.shared ? q.Rs : q.Rr));
         if (ld_acquire_gpu(done1 + tl.seg) < need) {
           const unsigned long long t0 = globaltimer();
           while (ld_acquire_gpu(done1 + tl.seg) < need) {
@@ -435,9 +677,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         }
         fence_proxy_async_global();  // the activations were written by other CTAs' generic stores
       }
+      if constexpr (F8) {
+        // every loader thread reads activations (and their row maxima) itself:
+        // order those loads after thread 0's acquire of the completion count
+        if (tl.phase == 1 && (p.phases & 1)) named_bar_sync(3, kTokThreads);
+      }
 
-      // ---- token rows of this thread for a gate/up tile: rows rbase + 16 j
-      const __nv_bfloat16 *src[BN / 16];
+      // ---- token rows of this thread for a gate/up tile: rows rbase + 16 j, as
+      // 16-byte pieces of 128-byte K-step rows (64 bf16 values, or with W8A8 the
+      // 128 E4M3 codes of the token's quantised row)
+      const uint8_t *src[BN / 16];
       if (tl.phase == 0) {
         bool bad = false;
 #pragma unroll
@@ -457,9 +706,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
               }
             }
           }
-          src[j] = p.hidden + (size_t)tok * p.H + c8 * 8;
+          src[j] = F8 ? p.hq + (size_t)tok * p.H + c8 * 16
+                      : reinterpret_cast<const uint8_t *>(p.hidden) + (size_t)tok * p.H * 2 + c8 * 16;
         }
         if (bad && err != nullptr) atomicOr(err, MOE_DEVERR_INDEX);
+      }
+      // W8A8 down tile: each activation row's scale from the row maxima the
+      // gate/up epilogue wrote per 32 columns (the 8 threads of a row split them)
+      float rsc[F8 ? BN / 16 : 1];
+      if constexpr (F8) {
+        if (tl.phase == 1) {
+          const int nb = (tl.shared ? p.Is : p.I) >> 5;
+          const float *am = tl.shared ? p.amax_s : p.amax;
+#pragma unroll
+          for (int j = 0; j < BN / 16; ++j) {
+            const int row = rbase + 16 * j;
+            float m = 0.0f;
+            if (row < tl.ntok)
+              for (int b = c8; b < nb; b += 8) m = fmaxf(m, __ldcg(am + (size_t)(tl.row0 + row) * nb + b));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            rsc[j] = e4m3_row_scale(m);
+          }
+        }
       }
       for (int kb = 0; kb < tl.nk; ++kb) {
         ok = __all_sync(0xffffffffu, mbar_wait(tempty_bar(ts), tph ^ 1u, err, abort_flag));
@@ -467,15 +737,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
           ok = false;
           break;
         }
-        const int k0 = kb * 64;
+        const int k0 = kb * KE;
         const uint32_t bs = t_smem(ts);
         if (tl.phase == 0) {
 #pragma unroll
           for (int j = 0; j < BN / 16; ++j) {
             const int row = rbase + 16 * j;
-            if (row < tl.N) cp_async_16(bs + row * 128 + ((c8 ^ (row & 7)) << 4), src[j] + k0);
+            if (row < tl.N) cp_async_16(bs + row * 128 + ((c8 ^ (row & 7)) << 4), src[j] + kb * 128);
           }
           cp_async_arrive_noinc(tfull_bar(ts));
+        } else if constexpr (F8) {
+          // W8A8 down tile: this thread's 16 activations of each of its rows,
+          // quantised with the row's scale into the 128-byte swizzled K-step row
+          // (rows past the segment's end are zero)
+          const int ld = tl.shared ? p.Is : p.I;
+          const __nv_bfloat16 *act = tl.shared ? p.act_s : p.act;
+#pragma unroll
+          for (int j = 0; j < BN / 16; ++j) {
+            const int row = rbase + 16 * j;
+            if (row < tl.N) {
+              uint4 o = make_uint4(0u, 0u, 0u, 0u);
+              if (row < tl.ntok) {
+                const uint4 *a = reinterpret_cast<const uint4 *>(act + (size_t)(tl.row0 + row) * ld + k0 + c8 * 16);
+                const uint4 v0 = __ldcg(a), v1 = __ldcg(a + 1);
+                const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                float f[16];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  f[2 * e] = __fdiv_rn(__uint_as_float(w[e] << 16), rsc[j]);
+                  f[2 * e + 1] = __fdiv_rn(__uint_as_float(w[e] & 0xFFFF0000u), rsc[j]);
+                }
+                o = make_uint4(e4m3_pack4(f[0], f[1], f[2], f[3]), e4m3_pack4(f[4], f[5], f[6], f[7]),
+                               e4m3_pack4(f[8], f[9], f[10], f[11]), e4m3_pack4(f[12], f[13], f[14], f[15]));
+              }
+              st_shared_v4(bs + row * 128 + ((c8 ^ (row & 7)) << 4), o);
+            }
+          }
+          fence_proxy_async_smem();  // generic-proxy writes read by the tensor core
+          mbar_arrive(tfull_bar(ts));
         } else if (tid == 0) {
           // activation rows row0 .. row0 + N (contiguous, N a multiple of 16 and
           // <= 256): boxes of 128 rows while they fit, then one each of 64/32/16
@@ -524,7 +823,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         const int t = ring[r];
         mbar_arrive(id_empty(r));
         if (t < 0) break;
-        const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+        const Tile tl = decode(t);
         const int acc = i % L::kAccBufs;
         const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
         ok = mbar_wait(aempty_bar(acc), aph ^ 1u, err, abort_flag);
@@ -532,11 +831,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         tc_fence_after();
         const uint32_t d0 = tmem + (uint32_t)(acc * 2 * BN);
         const uint32_t d1 = d0 + (uint32_t)BN;
-        const uint32_t idesc = idesc_bf16(128, tl.N);
+        const uint32_t idesc = F8 ? idesc_e4m3(128, tl.N) : idesc_bf16(128, tl.N);
         for (int kb = 0; kb < tl.nk; ++kb) {
           ok = mbar_wait(wfull_bar(ws), wph, err, abort_flag) && mbar_wait(tfull_bar(ts), tph, err, abort_flag);
           if (!ok) break;
-          if (tl.phase == 0) fence_proxy_async_smem();  // token rows were written by cp.async
+          if (tl.phase == 0 || F8) fence_proxy_async_smem();  // token rows were written by cp.async / stores
           tc_fence_after();
           const uint64_t a0 = sdesc_sw128(w_smem(ws));
           const uint64_t a1 = sdesc_sw128(w_smem(ws) + 16384);
@@ -544,8 +843,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-            umma_bf16(d0, a0 + 2 * kk, bd + 2 * kk, idesc, accum);
-            umma_bf16(d1, a1 + 2 * kk, bd + 2 * kk, idesc, accum);
+            if constexpr (F8) {  // 32 codes of K per MMA (32 bytes, as 16 bf16 values)
+              umma_f8(d0, a0 + 2 * kk, bd + 2 * kk, idesc, accum);
+              umma_f8(d1, a1 + 2 * kk, bd + 2 * kk, idesc, accum);
+            } else {
+              umma_bf16(d0, a0 + 2 * kk, bd + 2 * kk, idesc, accum);
+              umma_bf16(d1, a1 + 2 * kk, bd + 2 * kk, idesc, accum);
+            }
           }
           any = true;
           umma_commit(wempty_bar(ws));
@@ -586,17 +890,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       __syncwarp();
       if (lane == 0) mbar_arrive(id_empty(rs));
       if (t < 0) break;
-      const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+      const Tile tl = decode(t);
       const int acc = i % L::kAccBufs;
       const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
       ok = __all_sync(0xffffffffu, mbar_wait(afull_bar(acc), aph, err, abort_flag));
       if (!ok) break;
       tc_fence_after();
+      if constexpr (F8) {  // the row maxima of a down tile's activations come from other CTAs' gate/up tiles
+        if (tl.phase == 1 && (p.phases & 1)) (void)ld_acquire_gpu(done1 + tl.seg);
+      }
       const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * 2 * BN);
       // FP8 weights: the accumulators hold sum(value(code) * x); this lane's
       // row scales turn them into the products with the weights
       float s0 = 1.0f, s1 = 1.0f;
-      if constexpr (Q8) {
+      if constexpr (Q8 || F8) {
         if (tl.phase == 0) {
           const int ii = tl.rb * 128 + r;
           if (ii < (tl.shared ? p.Is : p.I)) {
@@ -697,7 +1004,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
               tmem_ld16(t0 + (uint32_t)c16, g);
               tmem_ld16(t0 + (uint32_t)(BN + c16), u);
               tmem_wait_ld();
-              if (ii < ld) {
+              if constexpr (F8) {
+                // W8A8: the accumulators hold code products; each row's weight scale
+                // and each column's token scale make them gate and up.  The bf16
+                // activation is stored, and its largest magnitude over this warp's
+                // 32 rows is kept per column for the down tiles' quantisation.
+                float cs = 0.0f;
+                const int cj = c16 + (lane & 15);
+                if (cj < tl.ntok) {
+                  int tok = tl.shared ? tl.row0 + cj : __ldg(p.perm + tl.row0 + cj) / p.top_k;
+                  tok = min(max(tok, 0), p.T - 1);
+                  cs = __ldg(p.hs + tok);
+                }
+                float m[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  const float csj = __shfl_sync(0xffffffffu, cs, j);
+                  m[j] = 0.0f;
+                  if (c16 + j < tl.ntok && ii < ld) {
+                    const __nv_bfloat16 b = __float2bfloat16_rn(silu_mul(g[j] * s0 * csj, u[j] * s1 * csj));
+                    out[(size_t)(tl.row0 + c16 + j) * ld + ii] = b;
+                    m[j] = fabsf(__bfloat162float(b));
+                  }
+                }
+                const int col = col_max16(m, lane);  // lane's column of the warp-wide maxima (in m[0])
+                if ((lane & 1) == 0 && c16 + col < tl.ntok)
+                  (tl.shared ? p.amax_s : p.amax)[(size_t)(tl.row0 + c16 + col) * (ld >> 5) + tl.rb * 4 + q] = m[0];
+              } else if (ii < ld) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                   if (c16 + j < tl.ntok)
@@ -730,12 +1063,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
               tmem_ld16(t0 + (uint32_t)c16, va);
               tmem_ld16(t0 + (uint32_t)(BN + c16), vb);
               tmem_wait_ld();
+              float cs = 1.0f;
+              if constexpr (F8) {
+                // each column's activation scale, as the loaders quantised it: its
+                // row's maximum over the per-32 maxima (two lanes per column)
+                const int nb = (tl.shared ? p.Is : p.I) >> 5;
+                const float *am = tl.shared ? p.amax_s : p.amax;
+                const int cj = c16 + (lane & 15);
+                float m = 0.0f;
+                if (cj < tl.ntok)
+                  for (int b = lane >> 4; b < nb; b += 2) m = fmaxf(m, __ldcg(am + (size_t)(tl.row0 + cj) * nb + b));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                cs = e4m3_row_scale(m);
+              }
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
+                const float csj = F8 ? __shfl_sync(0xffffffffu, cs, j) : 1.0f;
                 if (c16 + j < tl.ntok) {
                   __nv_bfloat16 *row = out + (size_t)(tl.row0 + c16 + j) * p.H;
-                  if (ha < p.H) __stcs(row + ha, __float2bfloat16_rn(Q8 ? va[j] * s0 : va[j]));
-                  if (hb < p.H) __stcs(row + hb, __float2bfloat16_rn(Q8 ? vb[j] * s1 : vb[j]));
+                  if (ha < p.H) __stcs(row + ha, __float2bfloat16_rn(Q8 ? va[j] * s0 : F8 ? va[j] * s0 * csj : va[j]));
+                  if (hb < p.H) __stcs(row + hb, __float2bfloat16_rn(Q8 ? vb[j] * s1 : F8 ? vb[j] * s1 * csj : vb[j]));
                 }
               }
             }
@@ -770,7 +1117,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       __syncwarp();
       if (lane == 0) mbar_arrive(id_empty(rs));
       if (t < 0) break;
-      const Tile tl = decode_tile<BN>(p, t, start1, start2, seg_off, nseg);
+      const Tile tl = decode(t);
       for (int kb = 0; kb < tl.nk; ++kb) {
         ok = __all_sync(0xffffffffu, mbar_wait(qfull_bar(qs), qph, err, abort_flag) &&
                                          mbar_wait(wempty_bar(ws), wph ^ 1u, err, abort_flag));
@@ -819,7 +1166,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
     if (prev == gridDim.x - 1) {
       volatile unsigned *s = p.sync;
       s[kSyncClaim] = 0;
-      for (int i = 0; i < nseg; ++i) s[kSyncDone + i] = 0;
+      for (int i = 0; i < p.E + p.has_shared; ++i) s[kSyncDone + i] = 0;
       __threadfence();
       s[kSyncExit] = 0;
     }
@@ -839,35 +1186,45 @@ int gemm_tile_n(int T, int top_k, int E) {
 }
 
 namespace {
-template <int BN, bool Q8>
+template <int BN, int MODE>
 cudaError_t launch_one(const GemmParams &p, int num_ctas, cudaStream_t stream, bool pdl) {
-  using L = Layout<BN, Q8>;
+  using L = Layout<BN, MODE>;
   static thread_local unsigned long long attr_ctx = 0;
-  const cudaError_t e = set_smem_attr_once((const void *)expert_ffn_kernel<BN, Q8>, (int)L::kSmem, attr_ctx);
+  const cudaError_t e = set_smem_attr_once((const void *)expert_ffn_kernel<BN, MODE>, (int)L::kSmem, attr_ctx);
   if (e != cudaSuccess) return e;
   void *args[] = {(void *)&p};
-  return launch_ex((const void *)expert_ffn_kernel<BN, Q8>, dim3(num_ctas), dim3(kGemmThreads), L::kSmem, stream, pdl, 1,
-                   args);
+  return launch_ex((const void *)expert_ffn_kernel<BN, MODE>, dim3(num_ctas), dim3(kGemmThreads), L::kSmem, stream,
+                   pdl, 1, args);
 }
 }  // namespace
 
 cudaError_t launch_expert_ffn(const GemmParams &p, int bn, int num_ctas, cudaStream_t stream, bool pdl) {
-  if (p.q8) {  // FP8 weights: narrow tiles only (the code ring takes the shared memory of wide token slots)
+  if (p.mode == kModeQ8) {  // weight-only FP8: narrow tiles only (the code ring takes the shared memory of wide token slots)
     switch (bn < 128 ? bn : 128) {
-      case 16: return launch_one<16, true>(p, num_ctas, stream, pdl);
-      case 32: return launch_one<32, true>(p, num_ctas, stream, pdl);
-      case 64: return launch_one<64, true>(p, num_ctas, stream, pdl);
-      case 128: return launch_one<128, true>(p, num_ctas, stream, pdl);
+      case 16: return launch_one<16, kModeQ8>(p, num_ctas, stream, pdl);
+      case 32: return launch_one<32, kModeQ8>(p, num_ctas, stream, pdl);
+      case 64: return launch_one<64, kModeQ8>(p, num_ctas, stream, pdl);
+      case 128: return launch_one<128, kModeQ8>(p, num_ctas, stream, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (p.mode == kModeF8) {  // W8A8: up to 240-token tiles (the epilogue has no staged form)
+    switch (bn < 240 ? bn : 240) {
+      case 16: return launch_one<16, kModeF8>(p, num_ctas, stream, pdl);
+      case 32: return launch_one<32, kModeF8>(p, num_ctas, stream, pdl);
+      case 64: return launch_one<64, kModeF8>(p, num_ctas, stream, pdl);
+      case 128: return launch_one<128, kModeF8>(p, num_ctas, stream, pdl);
+      case 240: return launch_one<240, kModeF8>(p, num_ctas, stream, pdl);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (bn) {
-    case 16: return launch_one<16, false>(p, num_ctas, stream, pdl);
-    case 32: return launch_one<32, false>(p, num_ctas, stream, pdl);
-    case 64: return launch_one<64, false>(p, num_ctas, stream, pdl);
-    case 128: return launch_one<128, false>(p, num_ctas, stream, pdl);
-    case 240: return launch_one<240, false>(p, num_ctas, stream, pdl);
-    case 256: return launch_one<256, false>(p, num_ctas, stream, pdl);
+    case 16: return launch_one<16, kModeBF16>(p, num_ctas, stream, pdl);
+    case 32: return launch_one<32, kModeBF16>(p, num_ctas, stream, pdl);
+    case 64: return launch_one<64, kModeBF16>(p, num_ctas, stream, pdl);
+    case 128: return launch_one<128, kModeBF16>(p, num_ctas, stream, pdl);
+    case 240: return launch_one<240, kModeBF16>(p, num_ctas, stream, pdl);
+    case 256: return launch_one<256, kModeBF16>(p, num_ctas, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

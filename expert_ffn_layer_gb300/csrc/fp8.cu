@@ -7,8 +7,7 @@
 // (1 for an all-zero row), code = E4M3 nearest-even of w / scale (fp32 IEEE
 // division), saturated at 448.  The expert kernel feeds the code values to the
 // MMAs and multiplies each row's fp32 accumulator by the row's scale.
-#include <cuda_fp8.h>
-
+#include "fp8.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -16,12 +15,6 @@ namespace moe {
 
 namespace {
 constexpr int kQThreads = 256;  // eight rows (one per warp) per CTA step
-
-__device__ __forceinline__ uint32_t pack4(float a, float b, float c, float d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return (lo & 0xFFFFu) | (hi << 16);
-}
 }  // namespace
 
 // One warp per row: the row maximum first, then the codes, 8 values per lane
@@ -46,7 +39,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(const __nv_bfl
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const float s = e4m3_row_scale(amax);
     if (lane == 0) scale[r] = s;
     uint2 *out = reinterpret_cast<uint2 *>(q + r * cols);
     for (int i = lane; i < n8; i += 32) {
@@ -58,7 +51,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(const __nv_bfl
         f[2 * j] = __fdiv_rn(__uint_as_float(u[j] << 16), s);
         f[2 * j + 1] = __fdiv_rn(__uint_as_float(u[j] & 0xFFFF0000u), s);
       }
-      out[i] = make_uint2(pack4(f[0], f[1], f[2], f[3]), pack4(f[4], f[5], f[6], f[7]));
+      out[i] = make_uint2(e4m3_pack4(f[0], f[1], f[2], f[3]), e4m3_pack4(f[4], f[5], f[6], f[7]));
     }
   }
 }

@@ -66,15 +66,29 @@ struct GemmParams {
   const int32_t *offsets;
   __nv_bfloat16 *act, *act_s;  // gate/up outputs: A_act [S][I], A_shared [T][Is]
   __nv_bfloat16 *y, *y_s;      // down outputs: y_sorted [S][H], y_shared [T][H]
-  // FP8 expert weights (q8 != 0): the weight maps above are uint8 maps of E4M3
-  // codes (box {64, 128, 1}, no swizzle) and these are the per-row fp32 scales
-  int q8;
+  // mode 0: bf16 weights.  FP8 expert weights: the weight maps above are uint8
+  // maps of E4M3 codes and sc_* the per-row fp32 scales; mode 1 (weight-only:
+  // boxes {64, 128, 1}, no swizzle, expanded to bf16 in shared memory) or
+  // mode 2 (W8A8: boxes {128, 128, 1}, 128-byte swizzle, FP8 MMAs on hq below)
+  int mode;
   const float *sc_g, *sc_u, *sc_d;     // [E][I], [E][I], [E][H]
   const float *sc_sg, *sc_su, *sc_sd;  // [Is], [Is], [H]
+  // W8A8 (mode 2): the hidden state quantised per token (codes [T][H], scales
+  // [T]), and the gate/up epilogue's per-32-column maxima of the bf16
+  // activations ([S][I/32] routed, [T][Is/32] shared) that set the down tiles'
+  // per-row activation scales
+  const uint8_t *hq;
+  const float *hs;
+  float *amax, *amax_s;
   unsigned *err;               // workspace error word
   unsigned *sync;              // workspace header: tile claim counter, exit counter, per-segment done counts
   int T, H, E, I, Is, top_k, S, has_shared;
   int phases;  // 1 gate/up only, 2 down only, 3 both (down tiles wait for their segment's gate/up tiles)
+  // 1: the shared expert's first gate/up tiles start before the previous
+  // kernel's results (perm, offsets) are awaited -- only when that kernel is
+  // this library's permutation, in the layer chain
+  int early;
+  int gu_order;  // gate/up claim order: 1 level-major (row block outermost), 0 segment-major
 };
 // word offsets into the workspace header (4 KiB, zero when the workspace is fresh;
 // every launch leaves them zero again)

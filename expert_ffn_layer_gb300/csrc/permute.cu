@@ -44,8 +44,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) permute_kernel(const PermutePar
   const int S = p.S, E = p.E;
   for (int i = threadIdx.x; i < kWarps * kMaxE; i += kThreads) (&base[0][0])[i] = 0;
 
-  pdl_wait();  // topk_idx comes from the router
-  pdl_launch_dependents();
+  pdl_launch_dependents();  // dependents wait for this kernel's completion themselves
+  pdl_wait();               // topk_idx comes from the router
   __syncthreads();
 
   const int chunk = (S + kWarps - 1) / kWarps;
@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(kPartThreads) permute_count_kernel(const Permu
   const int g = blockIdx.x, G = gridDim.x, E = p.E;
   for (int e = threadIdx.x; e < kMaxE; e += kPartThreads) cnt[e] = 0;
 
-  pdl_wait();  // topk_idx comes from the router
-  pdl_launch_dependents();
+  pdl_launch_dependents();  // dependents wait for this kernel's completion themselves
+  pdl_wait();               // topk_idx comes from the router
   __syncthreads();
 
   const int s0 = g * kPartSlots, s1 = min(p.S, s0 + kPartSlots);
@@ -254,8 +254,8 @@ __global__ void __launch_bounds__(kPartThreads) permute_scatter_kernel(const Per
   const int g = blockIdx.x, E = p.E;
   for (int i = threadIdx.x; i < kPartWarps * kMaxE; i += kPartThreads) (&base[0][0])[i] = 0;
 
-  pdl_wait();  // the table and topk_idx come from the count kernel and the router
   pdl_launch_dependents();
+  pdl_wait();  // the table and topk_idx come from the count kernel and the router
   __syncthreads();
 
   const int s0 = g * kPartSlots, s1 = min(p.S, s0 + kPartSlots);

@@ -119,8 +119,8 @@ __global__ void __launch_bounds__(kRouterThreads, 1) router_gemm_kernel(const __
   const uint32_t tmem = *tmem_slot;
   unsigned *err = p.err;
 
-  pdl_wait();  // W_high / W_low come from the split kernel
-  pdl_launch_dependents();
+  pdl_launch_dependents();  // dependents wait for this kernel's completion themselves
+  pdl_wait();               // W_high / W_low come from the split kernel
 
   bool ok = true;
   if (warp == 0) {
@@ -296,8 +296,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const __grid_constant_
   const int t0 = blockIdx.x * TPC;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = p.E;
-  pdl_wait();  // the partial logits come from the gemm kernel
   pdl_launch_dependents();
+  pdl_wait();  // the partial logits come from the gemm kernel
   const size_t stride = (size_t)p.T * E;
   // this thread's (token, expert) pairs i = tid + 256 j; every partial of every
   // pair in flight together, then each pair added in slice order

@@ -281,6 +281,28 @@ moe_status moe_layer_forward_fp8(const moe_dims *d, const moe_bf16 *hidden, cons
                                  const float *expert_bias, const moe_fp8_experts *w, moe_bf16 *out, void *ws,
                                  size_t ws_bytes, void *stream);
 
+/* W8A8: FP8 expert weights (moe_fp8_experts, as above) AND FP8 activations,
+ * multiplied on the tensor cores' 8-bit path.  [case] section 3 quantises the
+ * activation right before the down GEMM in its W8A8 deployments; the pages fix
+ * no format.  Reading: every activation matrix feeding an expert GEMM is
+ * quantised per row by the weight rule (E4M3, scale = max|row| / 448, codes
+ * nearest-even of value / scale) from its own values at run time -- the hidden
+ * state per token before the gate/up GEMM, and the bf16 SiLU(gate) * up
+ * activation per routed slot (per token for the shared expert) as the down
+ * GEMM loads it.  Each output element is (sum of code products) * row scale *
+ * column scale, accumulated in fp32.  The router stays fp32.
+ *   Shapes: H, I and I_shared multiples of 128 (else MOE_ERR_UNSUPPORTED).
+ *   moe_expert_ffn_w8a8: arguments and results as for moe_expert_ffn_fp8; it
+ *   first quantises `hidden` into the workspace, then runs the expert kernel.
+ *   moe_layer_forward_w8a8: quantisation of `hidden`, moe_route, moe_permute,
+ *   the W8A8 expert kernel and moe_combine on `stream`, intermediates in `ws`. */
+moe_status moe_expert_ffn_w8a8(const moe_dims *d, const moe_bf16 *hidden, const int32_t *perm,
+                               const int32_t *offsets, const moe_fp8_experts *w, moe_bf16 *y_sorted,
+                               moe_bf16 *y_shared, void *ws, size_t ws_bytes, void *stream);
+moe_status moe_layer_forward_w8a8(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,
+                                  const float *expert_bias, const moe_fp8_experts *w, moe_bf16 *out, void *ws,
+                                  size_t ws_bytes, void *stream);
+
 /* The whole layer (a1-a9) chained on `stream` with programmatic dependent
  * launch; every intermediate lives in `ws`.  Arguments as above; out [T, H] bf16. */
 moe_status moe_layer_forward(const moe_dims *d, const moe_bf16 *hidden, const float *router_w,

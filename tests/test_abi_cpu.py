@@ -63,9 +63,10 @@ def test_workspace_bytes(lib):
     S = 4096 * 8
     # dominated by y_sorted [S,H], y_shared [T,H], A_act [S,I], A_shared [T,I]
     # (bf16); the rest (routing tables, the router's bf16 weight halves and its
-    # split-K partial logits) is a few tens of MB
+    # split-K partial logits, the W8A8 path's quantised hidden state and
+    # activation row maxima) is a few tens of MB
     core = 2 * (S * 4096 + 4096 * 4096 + S * 1536 + 4096 * 1536)
-    assert core <= n <= core + (32 << 20)
+    assert core <= n <= core + (64 << 20)
     assert n % 256 == 0
     assert moe.moe_workspace_bytes(_hy3(8)) < n
     assert lib.moe_workspace_bytes(ctypes.byref(moe.dims(8, 4000, 192, 1536, 8))) == 0
@@ -83,6 +84,11 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
     assert lib.moe_fused_moe(byref(d), *([None] * 9), 0, None) == 1
     assert lib.moe_expert_ffn_fp8(byref(d), None, None, None, None, None, None, None, 0, None) == 1
     assert lib.moe_layer_forward_fp8(byref(d), None, None, None, None, None, None, 0, None) == 1
+    assert lib.moe_expert_ffn_w8a8(byref(d), None, None, None, None, None, None, None, 0, None) == 1
+    assert lib.moe_layer_forward_w8a8(byref(d), None, None, None, None, None, None, 0, None) == 1
+    # W8A8 needs H, I and I_shared multiples of 128 (checked before any pointer)
+    assert lib.moe_expert_ffn_w8a8(byref(moe.dims(8, 192, 4, 64, 2)), None, None, None, None, None, None, None, 0,
+                                   None) == 2
     assert lib.moe_quantize_fp8_rows(None, 4, 12, None, None, None) == 1      # cols % 8
     assert lib.moe_quantize_fp8_rows(None, 0, 16, None, None, None) == 0      # nothing to do
     # an FP8 weight struct with a missing scale array is rejected before launch
