@@ -714,6 +714,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       // W8A8 down tile: each activation row's scale from the row maxima the
       // gate/up epilogue wrote per 32 columns (the 8 threads of a row split them)
       float rsc[F8 ? BN / 16 : 1];
+      // narrow W8A8 down tiles (one or two rows per thread): the next K step's
+      // activations are loaded while this one is converted, so each step does
+      // not wait a full L2 round trip (wider tiles have enough loads per step)
+      constexpr int kPf = F8 && BN <= 32 ? BN / 16 : 0;
+      uint4 pf[kPf > 0 ? kPf : 1][2];
+      auto act_src = [&](int j, int kb) {
+        const int ld = tl.shared ? p.Is : p.I;
+        return reinterpret_cast<const uint4 *>((tl.shared ? p.act_s : p.act) + (size_t)(tl.row0 + rbase + 16 * j) * ld +
+                                               kb * KE + c8 * 16);
+      };
       if constexpr (F8) {
         if (tl.phase == 1) {
           const int nb = (tl.shared ? p.Is : p.I) >> 5;
@@ -729,9 +739,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
             rsc[j] = e4m3_row_scale(m);
           }
+#pragma unroll
+          for (int j = 0; j < kPf; ++j)
+            if (rbase + 16 * j < tl.ntok) {
+              pf[j][0] = __ldcg(act_src(j, 0));
+              pf[j][1] = __ldcg(act_src(j, 0) + 1);
+            }
         }
       }
       for (int kb = 0; kb < tl.nk; ++kb) {
+        uint4 cur[kPf > 0 ? kPf : 1][2];
+        if constexpr (kPf > 0) {
+          if (tl.phase == 1) {
+#pragma unroll
+            for (int j = 0; j < kPf; ++j) {
+              cur[j][0] = pf[j][0];
+              cur[j][1] = pf[j][1];
+              if (kb + 1 < tl.nk && rbase + 16 * j < tl.ntok) {
+                pf[j][0] = __ldcg(act_src(j, kb + 1));
+                pf[j][1] = __ldcg(act_src(j, kb + 1) + 1);
+              }
+            }
+          }
+        }
         ok = __all_sync(0xffffffffu, mbar_wait(tempty_bar(ts), tph ^ 1u, err, abort_flag));
         if (!ok || *abort_flag) {
           ok = false;
@@ -750,16 +780,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
           // W8A8 down tile: this thread's 16 activations of each of its rows,
           // quantised with the row's scale into the 128-byte swizzled K-step row
           // (rows past the segment's end are zero)
-          const int ld = tl.shared ? p.Is : p.I;
-          const __nv_bfloat16 *act = tl.shared ? p.act_s : p.act;
 #pragma unroll
           for (int j = 0; j < BN / 16; ++j) {
             const int row = rbase + 16 * j;
             if (row < tl.N) {
               uint4 o = make_uint4(0u, 0u, 0u, 0u);
               if (row < tl.ntok) {
-                const uint4 *a = reinterpret_cast<const uint4 *>(act + (size_t)(tl.row0 + row) * ld + k0 + c8 * 16);
-                const uint4 v0 = __ldcg(a), v1 = __ldcg(a + 1);
+                uint4 v0, v1;
+                if (j < kPf) {
+                  v0 = cur[j < kPf ? j : 0][0];
+                  v1 = cur[j < kPf ? j : 0][1];
+                } else {
+                  v0 = __ldcg(act_src(j, kb));
+                  v1 = __ldcg(act_src(j, kb) + 1);
+                }
                 const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
                 float f[16];
 #pragma unroll

@@ -483,7 +483,7 @@ def _sample_rows(T, n=24, seed=11):
     return np.unique(np.concatenate([np.arange(4), mid, np.arange(T - 4, T)]))
 
 
-@pytest.mark.parametrize("name", ["prefill", "zipf", "image"])
+@pytest.mark.parametrize("name", ["prefill", "prefill_u", "zipf", "image"])
 def test_layer_full_size_sampled(name):
     w = W.WORKLOADS[name]
     inp = W.layer_inputs(w)
@@ -507,6 +507,35 @@ def test_layer_full_size_sampled(name):
     (r, m), nties = _check_layer_rows(w, inp, got, rows, gi[rows])
     print(f"{name}: sampled rows {len(rows)} rel_l2={r:.3e} max_abs={m:.3e} near-tie rows={nties}; "
           f"expert counts max={c.max()} min={c.min()} empty={(c == 0).sum()}")
+    assert moe.moe_ws_read_error(dl.ws) == 0
+
+
+@pytest.mark.parametrize("name", ["prefill", "zipf", "image"])
+def test_full_size_whole_segments_and_shared(name):
+    """At full size, element by element: the whole y_sorted segment of the
+    largest, a median and the smallest non-empty expert (every chunk, the ragged
+    last one included) and all of y_shared, against the oracle's expert FFN on
+    the same token rows (the GPU's own routing, which the sampled-layer test and
+    the permutation tests check separately)."""
+    w = W.WORKLOADS[name]
+    inp = W.layer_inputs(w)
+    dl = DeviceLayer(w, inp)
+    idx, _, _ = dl.route()
+    counts, offsets, perm, inv = dl.permute(idx)
+    y, z = dl.expert_ffn(perm, offsets)
+    torch.cuda.synchronize()
+    c, o, p = counts.cpu().numpy(), offsets.cpu().numpy(), perm.cpu().numpy()
+    nz = np.nonzero(c)[0]
+    by = nz[np.argsort(c[nz], kind="stable")]
+    picks = sorted({int(by[-1]), int(by[len(by) // 2]), int(by[0])})
+    x = inp["hidden"]
+    for e in picks:
+        lo, hi = int(o[e]), int(o[e + 1])
+        tok = p[lo:hi] // w.top_k
+        ref = oracle.swiglu(x[tok], inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e])
+        assert_layer_close(host_f64(y[lo:hi]), ref, f"{name} expert {e} ({hi - lo} tokens) y_sorted")
+    ref_z = oracle.shared_expert(x, inp["ws_gate"], inp["ws_up"], inp["ws_down"])
+    assert_layer_close(host_f64(z), ref_z, f"{name} y_shared")
     assert moe.moe_ws_read_error(dl.ws) == 0
 
 
