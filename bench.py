@@ -356,16 +356,36 @@ def run_ours(args, rank, world, local_rank):
     w, d, layer, hidden, hidden_np, host = setup(name, rank)
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
     if args.profile:
-        if args.fp8:  # the same layer with FP8 expert weights (quantised once, before the layers)
+        if args.fp8 or args.w8a8:  # the layer with FP8 expert weights (quantised once, before the layers)
             q = moe.quantize_fp8_experts(layer.w_gate, layer.w_up, layer.w_down, layer.ws_gate, layer.ws_up,
                                          layer.ws_down)
+            fwd = moe.moe_layer_forward_w8a8 if args.w8a8 else moe.moe_layer_forward_fp8
             for _ in range(args.warmup + 1):
-                moe.moe_layer_forward_fp8(d, hidden, layer.router_w, layer.expert_bias, q, out, layer.ws)
+                fwd(d, hidden, layer.router_w, layer.expert_bias, q, out, layer.ws)
+        elif args.phases:
+            # warm-up layers, then the expert FFN's two phases as separate launches
+            # (gate/up, then down) so that counters can be taken per phase
+            for _ in range(args.warmup):
+                layer(hidden, out)
+            S = w.T * w.top_k
+            idx = torch.empty((w.T, w.top_k), dtype=torch.int32, device=dev)
+            wts = torch.empty((w.T, w.top_k), dtype=torch.float32, device=dev)
+            offs = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+            perm = torch.empty(S, dtype=torch.int32, device=dev)
+            moe.moe_route(d, hidden, layer.router_w, layer.expert_bias, idx, wts, layer.ws)
+            moe.moe_permute(d, idx, torch.empty(w.E, dtype=torch.int32, device=dev), offs, perm,
+                            torch.empty(S, dtype=torch.int32, device=dev), layer.ws)
+            y = torch.empty((S, w.H), dtype=torch.bfloat16, device=dev)
+            z = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+            moe.moe_expert_gate_up(d, hidden, perm, offs, layer.w_gate, layer.w_up, layer.ws_gate, layer.ws_up,
+                                   layer.ws)
+            moe.moe_expert_down(d, offs, layer.w_down, layer.ws_down, y, z, layer.ws)
         else:
             for _ in range(args.warmup + 1):
                 layer(hidden, out)
         torch.cuda.synchronize()
-        return {"profile": name, "fp8": bool(args.fp8), "device_error": moe.moe_ws_read_error(layer.ws)}
+        return {"profile": name, "fp8": bool(args.fp8), "w8a8": bool(args.w8a8), "phases": bool(args.phases),
+                "device_error": moe.moe_ws_read_error(layer.ws)}
 
     def eager_step():
         layer(hidden, out)
@@ -750,6 +770,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-weight decode measurement")
     ap.add_argument("--fp8", action="store_true", help="with --profile: run the layer with FP8 expert weights")
+    ap.add_argument("--w8a8", action="store_true", help="with --profile: run the W8A8 layer (FP8 weights and activations)")
+    ap.add_argument("--phases", action="store_true",
+                    help="with --profile: after the warm-up layers, run the expert FFN's gate/up and down as two launches")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -70,9 +70,9 @@ namespace {
 
 constexpr int kABytes = 2 * 128 * 128;  // weights of one K step: two 128-row x 64-bf16 boxes
 constexpr int kMaxSeg = 258;            // E <= 256 routed + 1 shared (+1 sentinel)
-// Runs of the claim order (see SchedTables): gate/up at most 2 per row-block
-// level (I <= 16384: 128 levels) + 2; down at most E + H / 256 = 256 + 64.
-constexpr int kMaxRuns = 580;
+// Gate/up runs of the claim order (the down phase's order has a closed form):
+// at most 1 + 256 (grouped level-major) or E + 2 (segment-major).
+constexpr int kMaxRuns = 260;
 // Shared-expert gate/up tiles claimed ahead of everything else (whole row-block
 // levels, at least one): in the layer chain they run before the routing is known.
 constexpr int kEarlyTiles = 32;
@@ -224,8 +224,8 @@ __device__ __forceinline__ Sched make_sched(const GemmParams &p) {
 // read by every role: schedule totals in shared memory.
 struct SchedMisc {
   int total;      // tiles of both phases
-  int n_gu_runs;  // runs [0, n_gu_runs) are gate/up, the rest down
-  int n_runs;
+  int n_gu_runs;  // gate/up runs (their tiles end at G1)
+  int G1;         // first down tile
 };
 
 template <int BN, int KSH>
@@ -238,14 +238,14 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const Sc
     seg = p.E;
     rb = t / q.nch_s;
     ch = t - rb * q.nch_s;
-  } else {
-    int lo = 0, hi = m.n_runs;  // the last run starting at or before t
+  } else if (t < m.G1) {
+    tl.phase = 0;
+    int lo = 0, hi = m.n_gu_runs;  // the last run starting at or before t (rstart[n_gu_runs] = G1)
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (rstart[mid] <= t) lo = mid;
       else hi = mid;
     }
-    tl.phase = lo < m.n_gu_runs ? 0 : 1;
     const int d = rdesc[lo];
     const int local = t - rstart[lo];
     if (d & kRunLevel) {
@@ -266,6 +266,33 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const Sc
       const int qq = local / nch;
       rb = run_rb(d) + qq;
       ch = local - qq * nch;
+    }
+  } else {
+    // down: routed segment s starts at Rd cst[s] + nsh(s) nch_s, with nsh(s) =
+    // floor(s nsd / E) shared row blocks placed before it; those placed after it
+    // follow its own tiles
+    tl.phase = 1;
+    const int u = t - m.G1;
+    const int nsd = p.has_shared ? q.Rd : 0;
+    auto dstart = [&](int x) { return q.Rd * cst[x] + (x * nsd / p.E) * q.nch_s; };
+    int a = 0, b = p.E;  // dstart(E) = every down tile > u
+    while (b - a > 1) {
+      const int mid = (a + b) >> 1;
+      if (dstart(mid) <= u) a = mid;
+      else b = mid;
+    }
+    const int nch = cst[a + 1] - cst[a];
+    const int end = dstart(a) + q.Rd * nch;
+    if (u < end) {
+      seg = a;
+      const int local = u - dstart(a);
+      rb = local / nch;
+      ch = local - rb * nch;
+    } else {
+      seg = p.E;
+      const int v = u - end;
+      rb = a * nsd / p.E + v / q.nch_s;
+      ch = v - (v / q.nch_s) * q.nch_s;
     }
   }
   tl.seg = seg;
@@ -371,28 +398,15 @@ __device__ void build_sched_tables(const GemmParams &p, const Sched &q, SchedMis
     }
   }
   G1 += q.Rr * C + max(0, q.Rs - q.r_e) * q.nch_s;
-  // ---- down runs: routed segments, shared row blocks spread between them
-  int n_runs = n_gu, total = G1;
-  if (q.Rd > 0) {
-    const int nsd = p.has_shared ? q.Rd : 0;
-    for (int s = lane; s < E; s += 32) {
-      const int nsh = min(nsd, (s * nsd) / E);  // shared row blocks placed before routed segment s
-      rstart[n_gu + s + nsh] = G1 + q.Rd * cst[s] + nsh * q.nch_s;
-      rdesc[n_gu + s + nsh] = run_desc(s, 0, q.Rd);
-    }
-    for (int dd = lane; dd < nsd; dd += 32) {
-      const int sd = ((dd + 1) * E + nsd - 1) / nsd - 1;  // placed after routed segment sd
-      rstart[n_gu + sd + 1 + dd] = G1 + q.Rd * cst[sd + 1] + dd * q.nch_s;
-      rdesc[n_gu + sd + 1 + dd] = run_desc(E, dd, 1);
-    }
-    n_runs += E + nsd;
-    total += q.Rd * C + nsd * q.nch_s;
-  }
+  // ---- down tiles: routed segments in order, the shared row blocks spread
+  // between them (closed form, see decode_tile)
+  int total = G1;
+  if (q.Rd > 0) total += q.Rd * C + (p.has_shared ? q.Rd : 0) * q.nch_s;
   if (lane == 0) {
-    rstart[n_runs] = total;
+    rstart[n_gu] = G1;
     m->total = total;
     m->n_gu_runs = n_gu;
-    m->n_runs = n_runs;
+    m->G1 = G1;
   }
   __threadfence_block();  // every lane's entries before lane 0 releases them (id_full)
   __syncwarp();
@@ -422,6 +436,18 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// max(p[first], p[first + step], ...) over indices < n, eight independent
+// loads per round (the maxima were written by other CTAs: loaded through L2)
+__device__ __forceinline__ float strided_max(const float *p, int first, int step, int n) {
+  float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int b = first; b < n; b += 8 * step) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (b + u * step < n) m[u] = fmaxf(m[u], __ldcg(p + b + u * step));
+  }
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
 
 // Column maxima of a warp's 32 rows x 16 columns: m[j] is this lane's value of
@@ -498,12 +524,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < KW; ++s) {
-      mbar_init(wfull_bar(s), Q8 ? kCvtWarps : 1);  // the weight loader's expect_tx arrival, or the converters
+      mbar_init(wfull_bar(s), Q8 ? kCvtWarps / 2 : 1);  // the weight loader's expect_tx arrival, or one converter group
       mbar_init(wempty_bar(s), 1);                  // MMA commit
     }
     for (int s = 0; s < KQ; ++s) {
       mbar_init(qfull_bar(s), 1);           // the loader's expect_tx arrival
-      mbar_init(qempty_bar(s), kCvtWarps);  // converters done reading
+      mbar_init(qempty_bar(s), kCvtWarps / 2);  // one converter group done reading
     }
     for (int s = 0; s < KT; ++s) {
       mbar_init(tfull_bar(s), kTokThreads);  // one arrival per loader thread (cp.async, or the TMA expect_tx)
@@ -731,9 +757,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
 #pragma unroll
           for (int j = 0; j < BN / 16; ++j) {
             const int row = rbase + 16 * j;
-            float m = 0.0f;
-            if (row < tl.ntok)
-              for (int b = c8; b < nb; b += 8) m = fmaxf(m, __ldcg(am + (size_t)(tl.row0 + row) * nb + b));
+            float m = row < tl.ntok ? strided_max(am + (size_t)(tl.row0 + row) * nb, c8, 8, nb) : 0.0f;
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
@@ -1104,9 +1128,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
                 const int nb = (tl.shared ? p.Is : p.I) >> 5;
                 const float *am = tl.shared ? p.amax_s : p.amax;
                 const int cj = c16 + (lane & 15);
-                float m = 0.0f;
-                if (cj < tl.ntok)
-                  for (int b = lane >> 4; b < nb; b += 2) m = fmaxf(m, __ldcg(am + (size_t)(tl.row0 + cj) * nb + b));
+                float m = cj < tl.ntok ? strided_max(am + (size_t)(tl.row0 + cj) * nb, lane >> 4, 2, nb) : 0.0f;
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
                 cs = e4m3_row_scale(m);
               }
@@ -1136,13 +1158,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   } else if constexpr (Q8) {
     // ================= FP8 weights (warps 14..21): codes -> bf16 weight slots
     // (the values of the codes; the epilogue applies each row's scale).
-    // Converter warp cw takes rows 32 (cw & 3) .. + 31 of box cw >> 2; per
+    // Two groups of four converter warps take alternate K steps (the per-step
+    // handoff -- waits, proxy fence, arrivals -- then overlaps across groups).
+    // Warp wg of a group converts rows 64 (wg & 1) .. + 63 of box wg >> 1; per
     // pass, lane l converts 16 codes (chunk l & 3) of row 8 it + (l >> 2), so a
     // warp reads 512 contiguous bytes and writes whole 128-byte swizzled rows.
+    // Parity waits stay unambiguous: with three weight slots a group's previous
+    // step (j - 2) needed MMA j - 5 done, which orders the slot's earlier phase
+    // (MMA j - 6) before its wait; with an even number of code slots, step
+    // j - KQ belonged to the same group.
+    static_assert(!Q8 || (KQ % 2 == 0 && KW == 3), "two converter groups need an even code ring and three weight slots");
     const int cw = warp - (kEpiWarp0 + EW);
-    const int box = cw >> 2, c = lane & 3;
+    const int grp = cw >> 2, wg = cw & 3;
+    const int box = wg >> 1, c = lane & 3;
     int ws = 0, qs = 0;
     uint32_t wph = 0, qph = 0;
+    unsigned kstep = 0;
     for (int i = 0; ok; ++i) {
       const int rs = i % kRing;
       ok = __all_sync(0xffffffffu, mbar_wait(id_full(rs), (uint32_t)(i / kRing) & 1u, err, abort_flag));
@@ -1152,28 +1183,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       if (lane == 0) mbar_arrive(id_empty(rs));
       if (t < 0) break;
       const Tile tl = decode(t);
-      for (int kb = 0; kb < tl.nk; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(qfull_bar(qs), qph, err, abort_flag) &&
-                                         mbar_wait(wempty_bar(ws), wph ^ 1u, err, abort_flag));
-        if (!ok) break;
-        const uint8_t *src = smem + L::kQOff + qs * kQBytes + box * (kQBytes / 2);
-        uint8_t *dst = smem + ws * kABytes + box * (kABytes / 2);
-        uint4 v[4];  // every read first: the stores cannot then hold back the next loads
+      for (int kb = 0; kb < tl.nk; ++kb, ++kstep) {
+        if ((int)(kstep & 1u) == grp) {
+          ok = __all_sync(0xffffffffu, mbar_wait(qfull_bar(qs), qph, err, abort_flag) &&
+                                           mbar_wait(wempty_bar(ws), wph ^ 1u, err, abort_flag));
+          if (!ok) break;
+          const uint8_t *src = smem + L::kQOff + qs * kQBytes + box * (kQBytes / 2);
+          uint8_t *dst = smem + ws * kABytes + box * (kABytes / 2);
+          uint4 v[8];  // every read first: the stores cannot then hold back the next loads
 #pragma unroll
-        for (int it = 0; it < 4; ++it)
-          v[it] = *reinterpret_cast<const uint4 *>(src + (32 * (cw & 3) + 8 * it + (lane >> 2)) * 64 + c * 16);
+          for (int it = 0; it < 8; ++it)
+            v[it] = *reinterpret_cast<const uint4 *>(src + (64 * (wg & 1) + 8 * it + (lane >> 2)) * 64 + c * 16);
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int rr = 32 * (cw & 3) + 8 * it + (lane >> 2);
-          *reinterpret_cast<uint4 *>(dst + rr * 128 + (((2 * c) ^ (rr & 7)) << 4)) = e4m3x8_to_bf16(v[it].x, v[it].y);
-          *reinterpret_cast<uint4 *>(dst + rr * 128 + (((2 * c + 1) ^ (rr & 7)) << 4)) =
-              e4m3x8_to_bf16(v[it].z, v[it].w);
-        }
-        fence_proxy_async_smem();  // generic-proxy writes read by the tensor core
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(wfull_bar(ws));
-          mbar_arrive(qempty_bar(qs));
+          for (int it = 0; it < 8; ++it) {
+            const int rr = 64 * (wg & 1) + 8 * it + (lane >> 2);
+            *reinterpret_cast<uint4 *>(dst + rr * 128 + (((2 * c) ^ (rr & 7)) << 4)) = e4m3x8_to_bf16(v[it].x, v[it].y);
+            *reinterpret_cast<uint4 *>(dst + rr * 128 + (((2 * c + 1) ^ (rr & 7)) << 4)) =
+                e4m3x8_to_bf16(v[it].z, v[it].w);
+          }
+          fence_proxy_async_smem();  // generic-proxy writes read by the tensor core
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(wfull_bar(ws));
+            mbar_arrive(qempty_bar(qs));
+          }
         }
         if (++ws == KW) {
           ws = 0;
