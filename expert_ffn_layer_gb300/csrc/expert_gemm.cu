@@ -51,7 +51,8 @@
 // Warp roles: 0 claims tiles and issues the weight TMA loads (lane 0) and
 // builds the claim-order tables once the routing is visible (whole warp); 1-4
 // load token rows (cp.async) or activation rows (TMA, one thread) and wait for
-// a down tile's gate/up tiles; 5 issues the MMAs (one thread) and owns TMEM;
+// a down tile's gate/up tiles; 5 and 22 issue the MMAs of the first and second
+// accumulator of the pair (one thread each; 5 owns TMEM);
 // 6-21 drain the accumulators, four warps per TMEM lane quarter taking its
 // 16-column groups in turn (the epilogue of a wide tile is not overlapped with
 // MMAs, so the more warps drain it the sooner TMEM is free: sixteen warps beat
@@ -80,10 +81,11 @@ constexpr int kGroupSegs = 32;  // routed segments per group of the level-major 
 constexpr int kWWarp = 0;               // tile claims + weight loads (lane 0)
 constexpr int kTokWarp0 = 1;            // warps 1-4: token / activation loads
 constexpr int kTokThreads = 128;
-constexpr int kMmaWarp = 5;
+constexpr int kMmaWarp = 5;             // issues the first accumulator's MMAs, owns TMEM
 constexpr int kEpiWarp0 = 6;            // warps 6.. : the epilogue
 constexpr int kEpiWarps = 16;
-constexpr int kGemmThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kMma2Warp = kEpiWarp0 + kEpiWarps;  // issues the second accumulator's MMAs
+constexpr int kGemmThreads = 32 * (kMma2Warp + 1);
 constexpr int kWideEpiCols = 16;        // epilogue column group of tiles of 64 tokens or more
 constexpr int kRing = 4;                // claimed tile ids in flight
 // FP8 weights: TMA brings the E4M3 codes of a K step (two 128-row x 64-code
@@ -125,7 +127,7 @@ struct Layout {
   static constexpr int kBarOff = kEpiOff + (kStageEpi ? kEpiW * kWideEpiCols * 64 : 0);  // tokens x 32 rows each
   // wfull, wempty per weight slot; tfull, tempty per token slot; acc full[2],
   // acc empty[2]; drain; id_full[kRing], id_empty[kRing]; qfull, qempty per code slot
-  static constexpr int kNumBars = 2 * kW + 2 * kT + 5 + 2 * kRing + 2 * kQ;
+  static constexpr int kNumBars = 2 * kW + 2 * kT + 6 + 2 * kRing + 2 * kQ;
   // tmem slot, abort flag, ring of tile ids, schedule scalars (SchedMisc)
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
   static constexpr int kSegOffOff = kMiscOff + 128;           // routed segment offsets [E + 1]
@@ -518,6 +520,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   auto id_empty = [&](int r) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + kRing + r]); };
   auto qfull_bar = [&](int s) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + 2 * kRing + s]); };
   auto qempty_bar = [&](int s) { return smem_u32(&bars[2 * KW + 2 * KT + 5 + 2 * kRing + KQ + s]); };
+  auto drain_bar2 = smem_u32(&bars[2 * KW + 2 * KT + 5 + 2 * kRing + 2 * KQ]);
   auto q_smem = [&](int s) { return smem_u32(smem + L::kQOff + s * kQBytes); };
   auto w_smem = [&](int s) { return smem_u32(smem + s * kABytes); };
   auto t_smem = [&](int s) { return smem_u32(smem + L::kTOff + s * L::kTokBytes); };
@@ -525,7 +528,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int s = 0; s < KW; ++s) {
       mbar_init(wfull_bar(s), Q8 ? kCvtWarps / 2 : 1);  // the weight loader's expect_tx arrival, or one converter group
-      mbar_init(wempty_bar(s), 1);                  // MMA commit
+      mbar_init(wempty_bar(s), 2);                  // both MMA issuers' commits
     }
     for (int s = 0; s < KQ; ++s) {
       mbar_init(qfull_bar(s), 1);           // the loader's expect_tx arrival
@@ -533,16 +536,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
     }
     for (int s = 0; s < KT; ++s) {
       mbar_init(tfull_bar(s), kTokThreads);  // one arrival per loader thread (cp.async, or the TMA expect_tx)
-      mbar_init(tempty_bar(s), 1);
+      mbar_init(tempty_bar(s), 2);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(afull_bar(a), 1);
+      mbar_init(afull_bar(a), 2);
       mbar_init(aempty_bar(a), EW);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(drain_bar2, 1);
     for (int r = 0; r < kRing; ++r) {
       mbar_init(id_full(r), 1);
-      mbar_init(id_empty(r), 1 + 4 + EW + (Q8 ? kCvtWarps : 0));  // MMA, token loaders, epilogue, converters
+      mbar_init(id_empty(r), 2 + 4 + EW + (Q8 ? kCvtWarps : 0));  // MMA issuers, token loaders, epilogue, converters
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -868,9 +872,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         for (int s = 0; s < KT; ++s)
           if ((issued >> s) & 1u) mbar_wait_drain(tfull_bar(s), (issued_par >> s) & 1u);
     }
-  } else if (warp == kMmaWarp) {
-    // ================= MMA issuer
+  } else if (warp == kMmaWarp || warp == kMma2Warp) {
+    // ================= MMA issuers: one thread per accumulator of the pair
+    // (gate / up rows, or the two 128-row halves of w_down).  A tcgen05.mma
+    // costs its issuing thread about 70 cycles whatever N is, so one thread
+    // issuing both accumulators' four MMAs per K step (and two commits) could
+    // not keep the tensor pipe busy below about N = 150; two threads issue in
+    // parallel.  Each commits to the slot barriers (two arrivals free a slot).
     if (lane == 0) {
+      const int half = warp == kMmaWarp ? 0 : 1;
       int ws = 0, ts = 0;
       uint32_t wph = 0, tph = 0;
       bool any = false;
@@ -887,27 +897,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         ok = mbar_wait(aempty_bar(acc), aph ^ 1u, err, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d0 = tmem + (uint32_t)(acc * 2 * BN);
-        const uint32_t d1 = d0 + (uint32_t)BN;
+        const uint32_t dh = tmem + (uint32_t)(acc * 2 * BN) + (uint32_t)(half * BN);
         const uint32_t idesc = F8 ? idesc_e4m3(128, tl.N) : idesc_bf16(128, tl.N);
         for (int kb = 0; kb < tl.nk; ++kb) {
           ok = mbar_wait(wfull_bar(ws), wph, err, abort_flag) && mbar_wait(tfull_bar(ts), tph, err, abort_flag);
           if (!ok) break;
           if (tl.phase == 0 || F8) fence_proxy_async_smem();  // token rows were written by cp.async / stores
           tc_fence_after();
-          const uint64_t a0 = sdesc_sw128(w_smem(ws));
-          const uint64_t a1 = sdesc_sw128(w_smem(ws) + 16384);
+          const uint64_t ah = sdesc_sw128(w_smem(ws) + (uint32_t)(half * 16384));
           const uint64_t bd = sdesc_sw128(t_smem(ts));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-            if constexpr (F8) {  // 32 codes of K per MMA (32 bytes, as 16 bf16 values)
-              umma_f8(d0, a0 + 2 * kk, bd + 2 * kk, idesc, accum);
-              umma_f8(d1, a1 + 2 * kk, bd + 2 * kk, idesc, accum);
-            } else {
-              umma_bf16(d0, a0 + 2 * kk, bd + 2 * kk, idesc, accum);
-              umma_bf16(d1, a1 + 2 * kk, bd + 2 * kk, idesc, accum);
-            }
+            if constexpr (F8) umma_f8(dh, ah + 2 * kk, bd + 2 * kk, idesc, accum);  // 32 codes of K per MMA
+            else umma_bf16(dh, ah + 2 * kk, bd + 2 * kk, idesc, accum);
           }
           any = true;
           umma_commit(wempty_bar(ws));
@@ -925,8 +928,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         umma_commit(afull_bar(acc));
       }
       if (!ok && any) {
-        umma_commit(drain_bar);
-        mbar_wait_drain(drain_bar, 0);
+        const uint32_t db = half == 0 ? drain_bar : drain_bar2;
+        umma_commit(db);
+        mbar_wait_drain(db, 0);
       }
     }
   } else if (warp < kEpiWarp0 + EW) {
