@@ -128,9 +128,11 @@ struct Layout {
   // wfull, wempty per weight slot; tfull, tempty per token slot; acc full[2],
   // acc empty[2]; drain; id_full[kRing], id_empty[kRing]; qfull, qempty per code slot
   static constexpr int kNumBars = 2 * kW + 2 * kT + 6 + 2 * kRing + 2 * kQ;
-  // tmem slot, abort flag, ring of tile ids, schedule scalars (SchedMisc)
+  // tmem slot, abort flag, ring of tile ids, schedule scalars (SchedMisc),
+  // then the decoded tiles of the ring (kRing x 32 bytes)
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
-  static constexpr int kSegOffOff = kMiscOff + 128;           // routed segment offsets [E + 1]
+  static constexpr int kTilesOff = kMiscOff + 128;
+  static constexpr int kSegOffOff = kTilesOff + 32 * kRing;   // routed segment offsets [E + 1]
   static constexpr int kCstOff = kSegOffOff + 4 * kMaxSeg;    // routed chunk prefix [E + 1]
   static constexpr int kRunStartOff = kCstOff + 4 * kMaxSeg;  // first tile of each run [runs + 1]
   static constexpr int kRunDescOff = kRunStartOff + 4 * (kMaxRuns + 1);
@@ -153,6 +155,7 @@ struct Tile {
   int phase;  // 0 gate/up, 1 down
   int seg, rb, row0, ntok, N, nk, shared;
 };
+static_assert(sizeof(Tile) == 32, "a ring entry of the decoded tiles");
 
 // Tokens per chunk for a segment of `cnt` tokens: the fewest chunks of at most
 // BN tokens, made as even as possible and rounded up to 16.
@@ -503,6 +506,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   volatile int *abort_flag = (volatile int *)(smem + L::kMiscOff + 4);
   volatile int *ring = (volatile int *)(smem + L::kMiscOff + 16);  // kRing claimed tile ids
   SchedMisc *misc = (SchedMisc *)(smem + L::kMiscOff + 32);
+  Tile *tiles = (Tile *)(smem + L::kTilesOff);  // the claimed tiles, decoded once by the claiming warp
   int *seg_off = (int *)(smem + L::kSegOffOff);
   int *cst = (int *)(smem + L::kCstOff);
   int *rstart = (int *)(smem + L::kRunStartOff);
@@ -623,13 +627,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         tables = true;
       }
       const int t = t0 < q.n_early ? t0 : (t0 < misc->total ? t0 : -1);
+      Tile tl;
       if (lane == 0) {
+        // the tile is decoded here, once, and published with its id: the other
+        // roles read the decoded entry instead of searching the run tables
+        if (t >= 0) {
+          tl = decode(t);
+          tiles[r] = tl;
+        }
         ring[r] = t;
-        mbar_arrive(id_full(r));  // release: the tables above are visible to the roles that take this id
+        mbar_arrive(id_full(r));  // release: the tables and the entry are visible to the roles that take this id
       }
       if (t < 0) break;
       if (lane == 0) {
-        const Tile tl = decode(t);
         const int i0 = tl.rb * (tl.phase == 0 ? 128 : 256);
         for (int kb = 0; kb < tl.nk; ++kb) {
           const uint32_t fb = Q8 ? qfull_bar(ws) : wfull_bar(ws);
@@ -681,6 +691,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       ok = __all_sync(0xffffffffu, mbar_wait(id_full(r), (uint32_t)(i / kRing) & 1u, err, abort_flag));
       if (!ok) break;
       const int t = ring[r];
+      const Tile tl = tiles[r];
       __syncwarp();
       if (lane == 0) mbar_arrive(id_empty(r));
       if (t < 0) break;
@@ -688,7 +699,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         pdl_wait();
         waited = true;
       }
-      const Tile tl = decode(t);
 
       // ---- a down tile needs every gate/up tile of its segment
       if (tl.phase == 1 && (p.phases & 1) && tid == 0) {
@@ -743,7 +753,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       }
       // W8A8 down tile: each activation row's scale from the row maxima the
       // gate/up epilogue wrote per 32 columns (the 8 threads of a row split them)
-      float rsc[F8 ? BN / 16 : 1];
+      float rsc[F8 ? BN / 16 : 1], rrc[F8 ? BN / 16 : 1];
       // narrow W8A8 down tiles (one or two rows per thread): the next K step's
       // activations are loaded while this one is converted, so each step does
       // not wait a full L2 round trip (wider tiles have enough loads per step)
@@ -766,6 +776,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
             rsc[j] = e4m3_row_scale(m);
+            rrc[j] = __frcp_rn(rsc[j]);
           }
 #pragma unroll
           for (int j = 0; j < kPf; ++j)
@@ -826,8 +837,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
                 float f[16];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                  f[2 * e] = __fdiv_rn(__uint_as_float(w[e] << 16), rsc[j]);
-                  f[2 * e + 1] = __fdiv_rn(__uint_as_float(w[e] & 0xFFFF0000u), rsc[j]);
+                  f[2 * e] = e4m3_quotient(__uint_as_float(w[e] << 16), rsc[j], rrc[j]);
+                  f[2 * e + 1] = e4m3_quotient(__uint_as_float(w[e] & 0xFFFF0000u), rsc[j], rrc[j]);
                 }
                 o = make_uint4(e4m3_pack4(f[0], f[1], f[2], f[3]), e4m3_pack4(f[4], f[5], f[6], f[7]),
                                e4m3_pack4(f[8], f[9], f[10], f[11]), e4m3_pack4(f[12], f[13], f[14], f[15]));
@@ -889,9 +900,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         ok = mbar_wait(id_full(r), (uint32_t)(i / kRing) & 1u, err, abort_flag);
         if (!ok) break;
         const int t = ring[r];
+        const Tile tl = tiles[r];
         mbar_arrive(id_empty(r));
         if (t < 0) break;
-        const Tile tl = decode(t);
         const int acc = i % L::kAccBufs;
         const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
         ok = mbar_wait(aempty_bar(acc), aph ^ 1u, err, abort_flag);
@@ -949,10 +960,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       ok = __all_sync(0xffffffffu, mbar_wait(id_full(rs), (uint32_t)(i / kRing) & 1u, err, abort_flag));
       if (!ok) break;
       const int t = ring[rs];
+      const Tile tl = tiles[rs];
       __syncwarp();
       if (lane == 0) mbar_arrive(id_empty(rs));
       if (t < 0) break;
-      const Tile tl = decode(t);
       const int acc = i % L::kAccBufs;
       const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
       ok = __all_sync(0xffffffffu, mbar_wait(afull_bar(acc), aph, err, abort_flag));
@@ -1183,10 +1194,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       ok = __all_sync(0xffffffffu, mbar_wait(id_full(rs), (uint32_t)(i / kRing) & 1u, err, abort_flag));
       if (!ok) break;
       const int t = ring[rs];
+      const Tile tl = tiles[rs];
       __syncwarp();
       if (lane == 0) mbar_arrive(id_empty(rs));
       if (t < 0) break;
-      const Tile tl = decode(t);
       for (int kb = 0; kb < tl.nk; ++kb, ++kstep) {
         if ((int)(kstep & 1u) == grp) {
           ok = __all_sync(0xffffffffu, mbar_wait(qfull_bar(qs), qph, err, abort_flag) &&

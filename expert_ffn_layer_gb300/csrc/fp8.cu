@@ -4,8 +4,8 @@
 // "Hy3 Preview inference optimisation case" lists W8A8 quantised deployments
 // and quantisation inside the FusedMoE chain without fixing a format.  Here:
 // OCP E4M3 codes (largest finite magnitude 448), scale = max|row| / 448 in fp32
-// (1 for an all-zero row), code = E4M3 nearest-even of w / scale (fp32 IEEE
-// division), saturated at 448.  The expert kernel feeds the code values to the
+// (1 for an all-zero row), code = E4M3 nearest-even of w / scale (the fp32
+// quotient rounded to nearest even), saturated at 448.  The expert kernel feeds the code values to the
 // MMAs and multiplies each row's fp32 accumulator by the row's scale.
 #include "fp8.cuh"
 #include "internal.h"
@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(const __nv_bfl
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = e4m3_row_scale(amax);
+    const float s = e4m3_row_scale(amax), rs = __frcp_rn(s);
     if (lane == 0) scale[r] = s;
     uint2 *out = reinterpret_cast<uint2 *>(q + r * cols);
     for (int i = lane; i < n8; i += 32) {
@@ -48,8 +48,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(const __nv_bfl
       float f[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        f[2 * j] = __fdiv_rn(__uint_as_float(u[j] << 16), s);
-        f[2 * j + 1] = __fdiv_rn(__uint_as_float(u[j] & 0xFFFF0000u), s);
+        f[2 * j] = e4m3_quotient(__uint_as_float(u[j] << 16), s, rs);
+        f[2 * j + 1] = e4m3_quotient(__uint_as_float(u[j] & 0xFFFF0000u), s, rs);
       }
       out[i] = make_uint2(e4m3_pack4(f[0], f[1], f[2], f[3]), e4m3_pack4(f[4], f[5], f[6], f[7]));
     }

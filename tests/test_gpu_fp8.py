@@ -86,6 +86,29 @@ def test_quantize_rows_bit_exact():
     assert np.array_equal(codes.cpu().numpy(), q_ref)
 
 
+def test_quantize_rows_bit_exact_wide_range():
+    """The device forms each quotient w / scale from one reciprocal per row and a
+    correction step; its codes equal the oracle's (fp32 division) on 2 M values
+    whose rows span twelve decades of scale and whose quotients span every E4M3
+    binade, subnormals included."""
+    rows, cols = 1024, 2048
+    rng = np.random.default_rng(7)
+    row_max = 10.0 ** rng.uniform(-7, 5, size=rows)
+    mag = row_max[:, None] * 2.0 ** rng.uniform(-16, 0, size=(rows, cols))
+    vals = np.where(rng.random((rows, cols)) < 0.5, -mag, mag).astype(np.float32)
+    vals[:, 0] = row_max.astype(np.float32)                      # the row's largest magnitude
+    w = (vals.view(np.uint32) >> 16).astype(np.uint16)          # truncation to bf16 keeps |v| <= max
+    src = bf16_dev(w)
+    codes = torch.empty(src.shape, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(rows, dtype=torch.float32, device="cuda")
+    moe.moe_quantize_fp8_rows(src, codes, scales)
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quantize_rows_e4m3(w)
+    assert np.array_equal(scales.cpu().numpy(), s_ref)
+    got = codes.cpu().numpy()
+    assert np.array_equal(got, q_ref), f"{int((got != q_ref).sum())} codes differ"
+
+
 @pytest.mark.parametrize("w", [W.WORKLOADS["tiny"], MID, MID_SOFTMAX, WIDE, ODD_H, NOSHARED, W.WORKLOADS["decode"]],
                          ids=["tiny", "mid", "mid_softmax", "wide", "odd_h", "noshared", "decode"])
 def test_expert_ffn_fp8_parity(w):
