@@ -25,6 +25,9 @@ WIDE = W.Workload("wide", 64, 256, 256, 16, 64, 64, "sigmoid", 2.826, 0.0, True,
 DENSE = W.Workload("dense", 37, 256, 1, 1, 128, 128, "sigmoid", 2.826, 0.0, True, "normal", 0.1, 8)
 ODD_H = W.Workload("odd_h", 20, 192, 4, 2, 64, 64, "sigmoid", 2.826, 0.0, True, "normal", 0.1, 9)
 NOSHARED = W.WORKLOADS["tiny"].with_(name="noshared", has_shared=False)
+# 32 tokens at top-16 over 64 experts: 512 routed slots, the permutation's
+# one-CTA form with every warp holding whole rounds of slots
+SMALL32 = W.Workload("small32", 32, 512, 64, 16, 128, 128, "sigmoid", 2.826, 0.0, True, "normal", 0.1, 11)
 SMALL = [W.WORKLOADS["tiny"], MID, MID_SOFTMAX, WIDE, DENSE, ODD_H, NOSHARED]
 SMALL_IDS = [w.name for w in SMALL]
 
@@ -121,12 +124,17 @@ def _router_only(w):
 
 @pytest.mark.parametrize("T,H,E,k,mode", [(128, 1024, 192, 8, "sigmoid"), (129, 1024, 192, 8, "sigmoid"),
                                           (100, 512, 256, 8, "softmax"), (1, 4096, 192, 8, "sigmoid"),
-                                          (77, 640, 48, 6, "sigmoid")])
+                                          (77, 640, 48, 6, "sigmoid"), (32, 4096, 192, 8, "sigmoid"),
+                                          (32, 512, 256, 16, "softmax"), (33, 4096, 192, 8, "sigmoid"),
+                                          (4100, 1024, 192, 8, "sigmoid"), (4100, 1024, 64, 8, "softmax")])
 def test_route_one_tile_and_boundary(T, H, E, k, mode):
     """A full 128-token tile, one token more (a second tile of one row), a
     single token, E = 256 (one 256-column accumulator pair), and H = 640 (ten K
-    slices: a split of two).  The router matches the oracle and repeats bit for
-    bit (the split-K partial logits are summed in a fixed order)."""
+    slices: a split of two); 32 and 33 tokens at the Hy3 shape, and 32 tokens
+    with E = 256 and top-16; 4100 tokens (the top-k kernel's eight-token CTAs,
+    four K slices, a ragged last tile) in both scoring modes.  The router
+    matches the oracle and repeats bit for bit (the split-K partial logits are
+    summed in a fixed order)."""
     w = W.Workload(f"r{T}_{H}_{E}", T, H, E, k, 128, 128, mode, 2.826 if mode == "sigmoid" else 1.0,
                    0.0 if mode == "sigmoid" else 1e-8, True, "normal" if mode == "sigmoid" else "none",
                    0.1 if mode == "sigmoid" else 0.0, 21)
@@ -422,7 +430,7 @@ def _check_layer_rows(w, inp, got_rows, rows, gpu_idx_rows):
     return assert_layer_close(got_rows, expected, f"{w.name} layer rows"), len(ties)
 
 
-@pytest.mark.parametrize("w", SMALL + [W.WORKLOADS["decode"]], ids=SMALL_IDS + ["decode"])
+@pytest.mark.parametrize("w", SMALL + [SMALL32, W.WORKLOADS["decode"]], ids=SMALL_IDS + ["small32", "decode"])
 def test_layer_parity(w):
     inp = inputs_of(w)
     dl = DeviceLayer(w, inp)
@@ -435,7 +443,8 @@ def test_layer_parity(w):
     assert moe.moe_ws_read_error(dl.ws) == 0
 
 
-@pytest.mark.parametrize("w", [W.WORKLOADS["tiny"], MID, W.WORKLOADS["decode"]], ids=["tiny", "mid", "decode"])
+@pytest.mark.parametrize("w", [W.WORKLOADS["tiny"], MID, SMALL32, W.WORKLOADS["decode"]],
+                         ids=["tiny", "mid", "small32", "decode"])
 def test_layer_equals_stage_chain_and_is_deterministic(w):
     inp = inputs_of(w)
     dl = DeviceLayer(w, inp)
