@@ -154,7 +154,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
   size_t err, topk_idx, topk_w, counts, offsets, perm, inv, perm_part, y_sorted, y_shared, a_act, a_shared, w_hi,
-      w_lo, partial, hq, hs, amax, amax_s, total;
+      w_lo, partial, hq, hs, amax, amax_s, aq, aq_s, asc, asc_s, total;
 };
 
 // Split of H across router CTAs: a power of two <= 32 dividing H/64, with
@@ -198,6 +198,11 @@ WsLayout ws_layout(const moe_dims &d) {
   L.hs = take(T * 4);
   L.amax = take(S * (size_t)(d.I / 32) * 4);
   L.amax_s = take(T * (size_t)(Is / 32) * 4);
+  // W8A8: the activations' E4M3 codes and their per-row scales (the quantisation tiles' output)
+  L.aq = take(S * (size_t)d.I);
+  L.aq_s = take(T * Is);
+  L.asc = take(S * 4);
+  L.asc_s = take(T * 4);
   L.total = off;
   return L;
 }
@@ -282,8 +287,10 @@ moe_status do_permute(const moe_dims &d, const int32_t *topk_idx, int32_t *count
 struct ExpertScratch {
   unsigned *hdr;
   __nv_bfloat16 *act, *act_s;
-  uint8_t *hq = nullptr;  // W8A8 only: the quantised hidden state and the activations' row maxima
+  uint8_t *hq = nullptr;  // W8A8 only: the quantised hidden state and the activations' row maxima,
   float *hs = nullptr, *amax = nullptr, *amax_s = nullptr;
+  uint8_t *aq = nullptr, *aq_s = nullptr;  // and the activations' codes and row scales
+  float *asc = nullptr, *asc_s = nullptr;
 };
 
 // the scratch inside a caller's workspace (moe_workspace_bytes layout)
@@ -297,6 +304,10 @@ ExpertScratch scratch_in(const moe_dims &d, void *ws) {
   sc.hs = at<float>(ws, L.hs);
   sc.amax = at<float>(ws, L.amax);
   sc.amax_s = at<float>(ws, L.amax_s);
+  sc.aq = at<uint8_t>(ws, L.aq);
+  sc.aq_s = at<uint8_t>(ws, L.aq_s);
+  sc.asc = at<float>(ws, L.asc);
+  sc.asc_s = at<float>(ws, L.asc_s);
   return sc;
 }
 
@@ -358,11 +369,19 @@ moe_status do_expert_phases(const moe_dims &d, int phases, const moe_bf16 *hidde
     g.hs = sc.hs;
     g.amax = sc.amax;
     g.amax_s = sc.amax_s;
+    g.aq = sc.aq;
+    g.aq_s = sc.aq_s;
+    g.asc = sc.asc;
+    g.asc_s = sc.asc_s;
     ok = map_u8_3d_sw(&g.map_wg, q->gate, d.H, d.I, d.E, 128) && map_u8_3d_sw(&g.map_wu, q->up, d.H, d.I, d.E, 128) &&
          map_u8_3d_sw(&g.map_wd, q->down, d.I, d.H, d.E, 128);
     if (d.has_shared)
       ok = ok && map_u8_2d_sw(&g.map_sg, q->s_gate, d.H, g.Is, 128) &&
            map_u8_2d_sw(&g.map_su, q->s_up, d.H, g.Is, 128) && map_u8_2d_sw(&g.map_sd, q->s_down, g.Is, d.H, 128);
+    // the down tiles load the activations' codes (128-code K steps) by TMA
+    for (int b = 0; b < 4; ++b) ok = ok && map_u8_2d_sw(&g.map_act[b], g.aq, d.I, g.S, 16u << b);
+    if (d.has_shared)
+      for (int b = 0; b < 4; ++b) ok = ok && map_u8_2d_sw(&g.map_acts[b], g.aq_s, g.Is, d.T, 16u << b);
     if (!ok) return MOE_ERR_CUDA;
     return cuda_status(launch_expert_ffn(g, bn, num_sms(), stream, pdl));
   }

@@ -152,7 +152,7 @@ struct Layout {
 };
 
 struct Tile {
-  int phase;  // 0 gate/up, 1 down
+  int phase;  // 0 gate/up, 1 down, 2 W8A8 activation quantisation of one chunk
   int seg, rb, row0, ntok, N, nk, shared;
 };
 static_assert(sizeof(Tile) == 32, "a ring entry of the decoded tiles");
@@ -228,9 +228,10 @@ __device__ __forceinline__ Sched make_sched(const GemmParams &p) {
 // Tables written once per CTA (by warp 0, after the routing is visible) and
 // read by every role: schedule totals in shared memory.
 struct SchedMisc {
-  int total;      // tiles of both phases
+  int total;      // tiles of all phases
   int n_gu_runs;  // gate/up runs (their tiles end at G1)
-  int G1;         // first down tile
+  int G1;         // first tile after the gate/up tiles (W8A8: the first quantisation tile)
+  int GD;         // first down tile (G1 unless W8A8)
 };
 
 template <int BN, int KSH>
@@ -238,6 +239,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const Sc
                                             const int *seg_off, const int *cst, const int *rstart, const int *rdesc) {
   Tile tl;
   int seg, rb, ch;
+  bool quant = false;
   if (t < q.n_early) {
     tl.phase = 0;
     seg = p.E;
@@ -272,12 +274,32 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const Sc
       rb = run_rb(d) + qq;
       ch = local - qq * nch;
     }
+  } else if (t < m.GD) {
+    // W8A8: one quantisation tile per chunk, routed segments in order, then the
+    // shared expert's chunks
+    tl.phase = 2;
+    quant = true;
+    rb = 0;
+    const int u = t - m.G1, C = cst[p.E];
+    if (u < C) {
+      int a = 0, b = p.E;  // the last segment whose chunks start at or before u
+      while (b - a > 1) {
+        const int mid = (a + b) >> 1;
+        if (cst[mid] <= u) a = mid;
+        else b = mid;
+      }
+      seg = a;
+      ch = u - cst[a];
+    } else {
+      seg = p.E;
+      ch = u - C;
+    }
   } else {
     // down: routed segment s starts at Rd cst[s] + nsh(s) nch_s, with nsh(s) =
     // floor(s nsd / E) shared row blocks placed before it; those placed after it
     // follow its own tiles
     tl.phase = 1;
-    const int u = t - m.G1;
+    const int u = t - m.GD;
     const int nsd = p.has_shared ? q.Rd : 0;
     auto dstart = [&](int x) { return q.Rd * cst[x] + (x * nsd / p.E) * q.nch_s; };
     int a = 0, b = p.E;  // dstart(E) = every down tile > u
@@ -309,7 +331,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const Sc
   tl.ntok = min(base, cnt - pin);
   tl.row0 = (tl.shared ? 0 : seg_off[seg]) + pin;
   tl.N = (tl.ntok + 15) & ~15;
-  tl.nk = tl.phase == 0 ? (p.H >> KSH) : ((tl.shared ? p.Is : p.I) >> KSH);  // K steps of 2^KSH
+  tl.nk = quant ? 0 : tl.phase == 0 ? (p.H >> KSH) : ((tl.shared ? p.Is : p.I) >> KSH);  // K steps of 2^KSH
   return tl;
 }
 
@@ -403,15 +425,18 @@ __device__ void build_sched_tables(const GemmParams &p, const Sched &q, SchedMis
     }
   }
   G1 += q.Rr * C + max(0, q.Rs - q.r_e) * q.nch_s;
+  // ---- W8A8: a quantisation tile per chunk between the gate/up and the down tiles
+  const int GD = G1 + (p.mode == 2 && q.Rd > 0 ? C + (p.has_shared ? q.nch_s : 0) : 0);
   // ---- down tiles: routed segments in order, the shared row blocks spread
   // between them (closed form, see decode_tile)
-  int total = G1;
+  int total = GD;
   if (q.Rd > 0) total += q.Rd * C + (p.has_shared ? q.Rd : 0) * q.nch_s;
   if (lane == 0) {
     rstart[n_gu] = G1;
     m->total = total;
     m->n_gu_runs = n_gu;
     m->G1 = G1;
+    m->GD = GD;
   }
   __threadfence_block();  // every lane's entries before lane 0 releases them (id_full)
   __syncwarp();
@@ -488,6 +513,47 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16(uint32_t w0, uint32_t w1) {
     o[j] = *reinterpret_cast<const uint32_t *>(&b);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// W8A8 quantisation tile: the activation rows of one chunk to E4M3 codes, once
+// (each down row block then loads the codes by TMA instead of quantising the
+// rows again).  Row scale = max |row| / 448 from the per-32-column maxima the
+// gate/up epilogue kept; the quotients as the row quantiser forms them.  The
+// 128 loader threads: rows rbase + 16 j, the 8 threads of a row taking its
+// 16-value pieces c8, c8 + 8, ...  Activations and maxima were written by other
+// CTAs: read through L2.
+template <int BN>
+__device__ __forceinline__ void quantize_chunk_rows(const GemmParams &p, const Tile &tl, int rbase, int c8) {
+  const int ld = tl.shared ? p.Is : p.I, nb = ld >> 5, npc = ld >> 4;
+  const float *am = tl.shared ? p.amax_s : p.amax;
+  const __nv_bfloat16 *act = tl.shared ? p.act_s : p.act;
+  uint8_t *codes = tl.shared ? p.aq_s : p.aq;
+  float *scales = tl.shared ? p.asc_s : p.asc;
+#pragma unroll 1
+  for (int j = 0; j < BN / 16; ++j) {
+    const int row = rbase + 16 * j;
+    float m = row < tl.ntok ? strided_max(am + (size_t)(tl.row0 + row) * nb, c8, 8, nb) : 0.0f;
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    if (row >= tl.ntok) continue;
+    const float sc = e4m3_row_scale(m), rs = __frcp_rn(sc);
+    if (c8 == 0) scales[tl.row0 + row] = sc;
+    const uint4 *src = reinterpret_cast<const uint4 *>(act + (size_t)(tl.row0 + row) * ld);
+    uint4 *dst = reinterpret_cast<uint4 *>(codes + (size_t)(tl.row0 + row) * ld);
+    for (int pc = c8; pc < npc; pc += 8) {
+      const uint4 v0 = __ldcg(src + 2 * pc), v1 = __ldcg(src + 2 * pc + 1);
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      float f[16];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        f[2 * e] = e4m3_quotient(__uint_as_float(w[e] << 16), sc, rs);
+        f[2 * e + 1] = e4m3_quotient(__uint_as_float(w[e] & 0xFFFF0000u), sc, rs);
+      }
+      dst[pc] = make_uint4(e4m3_pack4(f[0], f[1], f[2], f[3]), e4m3_pack4(f[4], f[5], f[6], f[7]),
+                           e4m3_pack4(f[8], f[9], f[10], f[11]), e4m3_pack4(f[12], f[13], f[14], f[15]));
+    }
+  }
 }
 
 }  // namespace
@@ -599,7 +665,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
   }
   unsigned *err = p.err;
   unsigned *claim = p.sync + kSyncClaim;
-  unsigned *done1 = p.sync + kSyncDone;  // gate/up tiles finished, per segment
+  unsigned *done1 = p.sync + kSyncDone;   // gate/up tiles finished, per segment
+  unsigned *done2 = p.sync + kSyncQuant;  // W8A8: quantisation tiles finished, per segment
   bool ok = true;
   auto decode = [&](int t) { return decode_tile<BN, KSH>(p, t, q, *misc, seg_off, cst, rstart, rdesc); };
 
@@ -713,13 +780,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         waited = true;
       }
 
-      // ---- a down tile needs every gate/up tile of its segment
-      if (tl.phase == 1 && (p.phases & 1) && tid == 0) {
+      // ---- a down tile needs every gate/up tile of its segment -- with W8A8,
+      // every quantisation tile of its segment, each of which needed those
+      if (tl.phase >= 1 && (p.phases & 1) && tid == 0) {
         const int nch = tl.shared ? q.nch_s : cst[tl.seg + 1] - cst[tl.seg];
-        const unsigned need = (unsigned)(nch * (tl.shared ? q.Rs : q.Rr));
-        if (ld_acquire_gpu(done1 + tl.seg) < need) {
+        const bool on_quant = F8 && tl.phase == 1;
+        const unsigned *cnt = (on_quant ? done2 : done1) + tl.seg;
+        const unsigned need = (unsigned)(on_quant ? nch : nch * (tl.shared ? q.Rs : q.Rr));
+        if (ld_acquire_gpu(cnt) < need) {
           const unsigned long long t0 = globaltimer();
-          while (ld_acquire_gpu(done1 + tl.seg) < need) {
+          while (ld_acquire_gpu(cnt) < need) {
             if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
               if (!*abort_flag && err != nullptr) atomicOr(err, MOE_DEVERR_TIMEOUT);
               *abort_flag = 1;
@@ -731,9 +801,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         fence_proxy_async_global();  // the activations were written by other CTAs' generic stores
       }
       if constexpr (F8) {
-        // every loader thread reads activations (and their row maxima) itself:
-        // order those loads after thread 0's acquire of the completion count
-        if (tl.phase == 1 && (p.phases & 1)) named_bar_sync(3, kTokThreads);
+        if (tl.phase == 2) {
+          // W8A8 quantisation tile: every loader thread reads activations and
+          // their row maxima itself, after thread 0's acquire of the count
+          named_bar_sync(3, kTokThreads);
+          quantize_chunk_rows<BN>(p, tl, rbase, c8);
+          __threadfence();  // the codes and scales, before the count (release)
+          named_bar_sync(3, kTokThreads);
+          if (tid == 0) atomicAdd(done2 + tl.seg, 1u);
+          continue;
+        }
       }
 
       // ---- token rows of this thread for a gate/up tile: rows rbase + 16 j, as
@@ -764,56 +841,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         }
         if (bad && err != nullptr) atomicOr(err, MOE_DEVERR_INDEX);
       }
-      // W8A8 down tile: each activation row's scale from the row maxima the
-      // gate/up epilogue wrote per 32 columns (the 8 threads of a row split them)
-      float rsc[F8 ? BN / 16 : 1], rrc[F8 ? BN / 16 : 1];
-      // narrow W8A8 down tiles (one or two rows per thread): the next K step's
-      // activations are loaded while this one is converted, so each step does
-      // not wait a full L2 round trip (wider tiles have enough loads per step)
-      constexpr int kPf = F8 && BN <= 32 ? BN / 16 : 0;
-      uint4 pf[kPf > 0 ? kPf : 1][2];
-      auto act_src = [&](int j, int kb) {
-        const int ld = tl.shared ? p.Is : p.I;
-        return reinterpret_cast<const uint4 *>((tl.shared ? p.act_s : p.act) + (size_t)(tl.row0 + rbase + 16 * j) * ld +
-                                               kb * KE + c8 * 16);
-      };
-      if constexpr (F8) {
-        if (tl.phase == 1) {
-          const int nb = (tl.shared ? p.Is : p.I) >> 5;
-          const float *am = tl.shared ? p.amax_s : p.amax;
-#pragma unroll
-          for (int j = 0; j < BN / 16; ++j) {
-            const int row = rbase + 16 * j;
-            float m = row < tl.ntok ? strided_max(am + (size_t)(tl.row0 + row) * nb, c8, 8, nb) : 0.0f;
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            rsc[j] = e4m3_row_scale(m);
-            rrc[j] = __frcp_rn(rsc[j]);
-          }
-#pragma unroll
-          for (int j = 0; j < kPf; ++j)
-            if (rbase + 16 * j < tl.ntok) {
-              pf[j][0] = __ldcg(act_src(j, 0));
-              pf[j][1] = __ldcg(act_src(j, 0) + 1);
-            }
-        }
-      }
       for (int kb = 0; kb < tl.nk; ++kb) {
-        uint4 cur[kPf > 0 ? kPf : 1][2];
-        if constexpr (kPf > 0) {
-          if (tl.phase == 1) {
-#pragma unroll
-            for (int j = 0; j < kPf; ++j) {
-              cur[j][0] = pf[j][0];
-              cur[j][1] = pf[j][1];
-              if (kb + 1 < tl.nk && rbase + 16 * j < tl.ntok) {
-                pf[j][0] = __ldcg(act_src(j, kb + 1));
-                pf[j][1] = __ldcg(act_src(j, kb + 1) + 1);
-              }
-            }
-          }
-        }
         ok = __all_sync(0xffffffffu, mbar_wait(tempty_bar(ts), tph ^ 1u, err, abort_flag));
         if (!ok || *abort_flag) {
           ok = false;
@@ -828,42 +856,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
             if (row < tl.N) cp_async_16(bs + row * 128 + ((c8 ^ (row & 7)) << 4), src[j] + kb * 128);
           }
           cp_async_arrive_noinc(tfull_bar(ts));
-        } else if constexpr (F8) {
-          // W8A8 down tile: this thread's 16 activations of each of its rows,
-          // quantised with the row's scale into the 128-byte swizzled K-step row
-          // (rows past the segment's end are zero)
-#pragma unroll
-          for (int j = 0; j < BN / 16; ++j) {
-            const int row = rbase + 16 * j;
-            if (row < tl.N) {
-              uint4 o = make_uint4(0u, 0u, 0u, 0u);
-              if (row < tl.ntok) {
-                uint4 v0, v1;
-                if (j < kPf) {
-                  v0 = cur[j < kPf ? j : 0][0];
-                  v1 = cur[j < kPf ? j : 0][1];
-                } else {
-                  v0 = __ldcg(act_src(j, kb));
-                  v1 = __ldcg(act_src(j, kb) + 1);
-                }
-                const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                float f[16];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  f[2 * e] = e4m3_quotient(__uint_as_float(w[e] << 16), rsc[j], rrc[j]);
-                  f[2 * e + 1] = e4m3_quotient(__uint_as_float(w[e] & 0xFFFF0000u), rsc[j], rrc[j]);
-                }
-                o = make_uint4(e4m3_pack4(f[0], f[1], f[2], f[3]), e4m3_pack4(f[4], f[5], f[6], f[7]),
-                               e4m3_pack4(f[8], f[9], f[10], f[11]), e4m3_pack4(f[12], f[13], f[14], f[15]));
-              }
-              st_shared_v4(bs + row * 128 + ((c8 ^ (row & 7)) << 4), o);
-            }
-          }
-          fence_proxy_async_smem();  // generic-proxy writes read by the tensor core
-          mbar_arrive(tfull_bar(ts));
         } else if (tid == 0) {
           // activation rows row0 .. row0 + N (contiguous, N a multiple of 16 and
-          // <= 256): boxes of 128 rows while they fit, then one each of 64/32/16
+          // <= 256; with W8A8 their E4M3 codes): boxes of 128 rows while they
+          // fit, then one each of 64/32/16
           mbar_arrive_expect_tx(tfull_bar(ts), (uint32_t)(tl.N * 128));
           issued |= 1u << ts;
           issued_par = (issued_par & ~(1u << ts)) | (tph << ts);
@@ -908,6 +904,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       int ws = 0, ts = 0;
       uint32_t wph = 0, tph = 0;
       bool any = false;
+      int na = 0;  // tiles that used an accumulator (quantisation tiles do not)
       for (int i = 0; ok; ++i) {
         const int r = i % kRing;
         ok = mbar_wait(id_full(r), (uint32_t)(i / kRing) & 1u, err, abort_flag);
@@ -916,8 +913,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         const Tile tl = tiles[r];
         mbar_arrive(id_empty(r));
         if (t < 0) break;
-        const int acc = i % L::kAccBufs;
-        const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
+        if (tl.phase == 2) continue;
+        const int acc = na % L::kAccBufs;
+        const uint32_t aph = (uint32_t)(na / L::kAccBufs) & 1u;
+        ++na;
         ok = mbar_wait(aempty_bar(acc), aph ^ 1u, err, abort_flag);
         if (!ok) break;
         tc_fence_after();
@@ -968,6 +967,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
     const int c_first = kEpiCols * ((warp - kEpiWarp0) >> 2);
     __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(smem + L::kEpiOff + (warp - kEpiWarp0) * kEpiCols * 64);
     const int r = 32 * q + lane;  // weight row within the 128-row half
+    int na = 0;  // tiles that used an accumulator (quantisation tiles do not)
     for (int i = 0; ok; ++i) {
       const int rs = i % kRing;
       ok = __all_sync(0xffffffffu, mbar_wait(id_full(rs), (uint32_t)(i / kRing) & 1u, err, abort_flag));
@@ -977,13 +977,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       __syncwarp();
       if (lane == 0) mbar_arrive(id_empty(rs));
       if (t < 0) break;
-      const int acc = i % L::kAccBufs;
-      const uint32_t aph = (uint32_t)(i / L::kAccBufs) & 1u;
+      if (tl.phase == 2) continue;
+      const int acc = na % L::kAccBufs;
+      const uint32_t aph = (uint32_t)(na / L::kAccBufs) & 1u;
+      ++na;
       ok = __all_sync(0xffffffffu, mbar_wait(afull_bar(acc), aph, err, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      if constexpr (F8) {  // the row maxima of a down tile's activations come from other CTAs' gate/up tiles
-        if (tl.phase == 1 && (p.phases & 1)) (void)ld_acquire_gpu(done1 + tl.seg);
+      if constexpr (F8) {  // a down tile's activation scales come from other CTAs' quantisation tiles
+        if (tl.phase == 1 && (p.phases & 1)) (void)ld_acquire_gpu(done2 + tl.seg);
       }
       const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * 2 * BN);
       // FP8 weights: the accumulators hold sum(value(code) * x); this lane's
@@ -1151,14 +1153,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
               tmem_wait_ld();
               float cs = 1.0f;
               if constexpr (F8) {
-                // each column's activation scale, as the loaders quantised it: its
-                // row's maximum over the per-32 maxima (two lanes per column)
-                const int nb = (tl.shared ? p.Is : p.I) >> 5;
-                const float *am = tl.shared ? p.amax_s : p.amax;
+                // each column's activation scale, as its quantisation tile stored it
                 const int cj = c16 + (lane & 15);
-                float m = cj < tl.ntok ? strided_max(am + (size_t)(tl.row0 + cj) * nb, lane >> 4, 2, nb) : 0.0f;
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-                cs = e4m3_row_scale(m);
+                if (cj < tl.ntok) cs = __ldcg((tl.shared ? p.asc_s : p.asc) + tl.row0 + cj);
               }
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -1262,6 +1259,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
       volatile unsigned *s = p.sync;
       s[kSyncClaim] = 0;
       for (int i = 0; i < p.E + p.has_shared; ++i) s[kSyncDone + i] = 0;
+      if (p.mode == kModeF8)
+        for (int i = 0; i < p.E + p.has_shared; ++i) s[kSyncQuant + i] = 0;
       __threadfence();
       s[kSyncExit] = 0;
     }

@@ -80,6 +80,11 @@ struct GemmParams {
   const uint8_t *hq;
   const float *hs;
   float *amax, *amax_s;
+  // W8A8: the activations' E4M3 codes ([S][I], [T][Is]; map_act / map_acts then
+  // describe these, boxes {128, 16/32/64/128}) and their per-row scales ([S], [T]),
+  // written by the quantisation tiles
+  uint8_t *aq, *aq_s;
+  float *asc, *asc_s;
   unsigned *err;               // workspace error word
   unsigned *sync;              // workspace header: tile claim counter, exit counter, per-segment done counts
   int T, H, E, I, Is, top_k, S, has_shared;
@@ -92,7 +97,9 @@ struct GemmParams {
 };
 // word offsets into the workspace header (4 KiB, zero when the workspace is fresh;
 // every launch leaves them zero again)
-constexpr int kSyncClaim = 64, kSyncExit = 65, kSyncPermute = 66, kSyncDone = 128;  // kSyncDone .. kSyncDone + 257
+constexpr int kSyncClaim = 64, kSyncExit = 65, kSyncPermute = 66,
+              kSyncDone = 128,   // kSyncDone .. + 257: gate/up tiles finished, per segment
+              kSyncQuant = 512;  // kSyncQuant .. + 257: W8A8 quantisation tiles finished, per segment
 constexpr int kWsHeaderBytes = 4096;
 int gemm_tile_n(int T, int top_k, int E);  // widest token tile (multiple of 16, <= 256) for a batch
 cudaError_t launch_expert_ffn(const GemmParams &p, int bn, int num_ctas, cudaStream_t stream, bool pdl);

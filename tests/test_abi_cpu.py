@@ -62,10 +62,11 @@ def test_workspace_bytes(lib):
     n = moe.moe_workspace_bytes(d)
     S = 4096 * 8
     # dominated by y_sorted [S,H], y_shared [T,H], A_act [S,I], A_shared [T,I]
-    # (bf16); the rest (routing tables, the router's bf16 weight halves and its
-    # split-K partial logits, the W8A8 path's quantised hidden state and
-    # activation row maxima) is a few tens of MB
-    core = 2 * (S * 4096 + 4096 * 4096 + S * 1536 + 4096 * 1536)
+    # (bf16) and the W8A8 path's activation codes [S,I], [T,I] (one byte each);
+    # the rest (routing tables, the router's bf16 weight halves and its split-K
+    # partial logits, the W8A8 path's quantised hidden state, activation row
+    # maxima and row scales) is a few tens of MB
+    core = 2 * (S * 4096 + 4096 * 4096 + S * 1536 + 4096 * 1536) + (S * 1536 + 4096 * 1536)
     assert core <= n <= core + (64 << 20)
     assert n % 256 == 0
     assert moe.moe_workspace_bytes(_hy3(8)) < n
