@@ -573,6 +573,18 @@ def run_ours(args, rank, world, local_rank):
             "gpu_launches": layer_launches(bw.T, bw.top_k) * args.steps,
             "clocks_under_load": bclk.summary(),
         }
+        if name == "prefill":
+            # the same layer with W8A8 experts (E4M3 weights, quantised once, and
+            # E4M3 activations; moe_layer_forward_w8a8), not the headline dtype
+            q8 = moe.quantize_fp8_experts(blayer.w_gate, blayer.w_up, blayer.w_down, blayer.ws_gate, blayer.ws_up,
+                                          blayer.ws_down)
+            wout = torch.empty_like(bout)
+            wg = graph_of(lambda: moe.moe_layer_forward_w8a8(bd, bhidden, blayer.router_w, blayer.expert_bias, q8,
+                                                             wout, blayer.ws), 1)
+            wms = float(np.mean(timed(wg.replay, args.steps, args.warmup)))
+            res["w8a8"] = {"value": round(bw.T / (wms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(wms, 5),
+                           "device_error": moe.moe_ws_read_error(blayer.ws)}
+            del q8, wg
         del blayer, bhidden, bgraph
         torch.cuda.empty_cache()
         return res

@@ -157,6 +157,16 @@ struct Tile {
 };
 static_assert(sizeof(Tile) == 32, "a ring entry of the decoded tiles");
 
+// W8A8 quantisation tiles per chunk row: one tile per 256 activation columns
+// when chunks are wide and experts average at most 256 tokens (the work of a
+// chunk then spreads over several SMs; Hy3 prefill 1.49 -> 1.13 ms), else one
+// per chunk (short chunks at decode, many chunks per expert on larger batches,
+// where the extra tiles cost more than they balance).
+template <int BN>
+__device__ __forceinline__ int quant_blocks(const GemmParams &p, int ld) {
+  return (BN >= 128 && p.S <= 256 * p.E) ? (ld + 255) >> 8 : 1;
+}
+
 // Tokens per chunk for a segment of `cnt` tokens: the fewest chunks of at most
 // BN tokens, made as even as possible and rounded up to 16.
 template <int BN>
@@ -279,20 +289,23 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams &p, int t, const Sc
     // shared expert's chunks
     tl.phase = 2;
     quant = true;
-    rb = 0;
-    const int u = t - m.G1, C = cst[p.E];
-    if (u < C) {
-      int a = 0, b = p.E;  // the last segment whose chunks start at or before u
+    const int u = t - m.G1, C = cst[p.E], Qr = quant_blocks<BN>(p, p.I), Qs = quant_blocks<BN>(p, p.Is);
+    if (u < C * Qr) {
+      const int cu = u / Qr;
+      rb = u - cu * Qr;  // the tile's block of activation columns
+      int a = 0, b = p.E;  // the last segment whose chunks start at or before cu
       while (b - a > 1) {
         const int mid = (a + b) >> 1;
-        if (cst[mid] <= u) a = mid;
+        if (cst[mid] <= cu) a = mid;
         else b = mid;
       }
       seg = a;
-      ch = u - cst[a];
+      ch = cu - cst[a];
     } else {
       seg = p.E;
-      ch = u - C;
+      const int v = u - C * Qr;
+      ch = v / Qs;
+      rb = v - ch * Qs;
     }
   } else {
     // down: routed segment s starts at Rd cst[s] + nsh(s) nch_s, with nsh(s) =
@@ -426,7 +439,9 @@ __device__ void build_sched_tables(const GemmParams &p, const Sched &q, SchedMis
   }
   G1 += q.Rr * C + max(0, q.Rs - q.r_e) * q.nch_s;
   // ---- W8A8: a quantisation tile per chunk between the gate/up and the down tiles
-  const int GD = G1 + (p.mode == 2 && q.Rd > 0 ? C + (p.has_shared ? q.nch_s : 0) : 0);
+  const int GD = G1 + (p.mode == 2 && q.Rd > 0 ? C * quant_blocks<BN>(p, p.I) +
+                                                       (p.has_shared ? q.nch_s * quant_blocks<BN>(p, p.Is) : 0)
+                                                 : 0);
   // ---- down tiles: routed segments in order, the shared row blocks spread
   // between them (closed form, see decode_tile)
   int total = GD;
@@ -515,7 +530,8 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16(uint32_t w0, uint32_t w1) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// W8A8 quantisation tile: the activation rows of one chunk to E4M3 codes, once
+// W8A8 quantisation tile: the activation rows of one chunk (or one block of 256
+// of their columns, see quant_blocks) to E4M3 codes, once
 // (each down row block then loads the codes by TMA instead of quantising the
 // rows again).  Row scale = max |row| / 448 from the per-32-column maxima the
 // gate/up epilogue kept; the quotients as the row quantiser forms them.  The
@@ -525,6 +541,8 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16(uint32_t w0, uint32_t w1) {
 template <int BN>
 __device__ __forceinline__ void quantize_chunk_rows(const GemmParams &p, const Tile &tl, int rbase, int c8) {
   const int ld = tl.shared ? p.Is : p.I, nb = ld >> 5, npc = ld >> 4;
+  const bool split = quant_blocks<BN>(p, ld) > 1;  // this tile covers 256 columns (16 pieces) of each row
+  const int pc0 = split ? tl.rb * 16 : 0, pc1 = split ? min(pc0 + 16, npc) : npc;
   const float *am = tl.shared ? p.amax_s : p.amax;
   const __nv_bfloat16 *act = tl.shared ? p.act_s : p.act;
   uint8_t *codes = tl.shared ? p.aq_s : p.aq;
@@ -538,10 +556,10 @@ __device__ __forceinline__ void quantize_chunk_rows(const GemmParams &p, const T
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
     if (row >= tl.ntok) continue;
     const float sc = e4m3_row_scale(m), rs = __frcp_rn(sc);
-    if (c8 == 0) scales[tl.row0 + row] = sc;
+    if (c8 == 0 && pc0 == 0) scales[tl.row0 + row] = sc;
     const uint4 *src = reinterpret_cast<const uint4 *>(act + (size_t)(tl.row0 + row) * ld);
     uint4 *dst = reinterpret_cast<uint4 *>(codes + (size_t)(tl.row0 + row) * ld);
-    for (int pc = c8; pc < npc; pc += 8) {
+    for (int pc = pc0 + c8; pc < pc1; pc += 8) {
       const uint4 v0 = __ldcg(src + 2 * pc), v1 = __ldcg(src + 2 * pc + 1);
       const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
       float f[16];
@@ -786,7 +804,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) expert_ffn_kernel(const __gri
         const int nch = tl.shared ? q.nch_s : cst[tl.seg + 1] - cst[tl.seg];
         const bool on_quant = F8 && tl.phase == 1;
         const unsigned *cnt = (on_quant ? done2 : done1) + tl.seg;
-        const unsigned need = (unsigned)(on_quant ? nch : nch * (tl.shared ? q.Rs : q.Rr));
+        const int nq = quant_blocks<BN>(p, tl.shared ? p.Is : p.I);  // quantisation tiles per chunk
+        const unsigned need = (unsigned)(on_quant ? nch * nq : nch * (tl.shared ? q.Rs : q.Rr));
         if (ld_acquire_gpu(cnt) < need) {
           const unsigned long long t0 = globaltimer();
           while (ld_acquire_gpu(cnt) < need) {

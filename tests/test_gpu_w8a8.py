@@ -80,8 +80,12 @@ def _fp8_dev(dl):
     return moe.quantize_fp8_experts(dl.w_gate, dl.w_up, dl.w_down, dl.ws_gate, dl.ws_up, dl.ws_down)
 
 
-SHAPES = [W.WORKLOADS["tiny"], MID, MID_SOFTMAX, NOSHARED, W.WORKLOADS["decode"]]
-SHAPE_IDS = ["tiny", "mid", "mid_softmax", "noshared", "decode"]
+# 240-token tiles with experts averaging at most 256 tokens and I = 768: the
+# quantisation of each chunk split into three 256-column tiles (the shared
+# expert's I = 640 into two whole blocks and a ragged one of 128 columns)
+MID_WIDE_I = MID.with_(name="mid_wide_i", I=768, I_shared=640)
+SHAPES = [W.WORKLOADS["tiny"], MID, MID_SOFTMAX, NOSHARED, MID_WIDE_I, W.WORKLOADS["decode"]]
+SHAPE_IDS = ["tiny", "mid", "mid_softmax", "noshared", "mid_wide_i", "decode"]
 
 
 @pytest.mark.parametrize("w", SHAPES, ids=SHAPE_IDS)
@@ -123,7 +127,8 @@ def test_expert_ffn_w8a8_skewed(T):
     assert moe.moe_ws_read_error(dl.ws) == 0
 
 
-@pytest.mark.parametrize("w", [W.WORKLOADS["tiny"], MID, W.WORKLOADS["decode"]], ids=["tiny", "mid", "decode"])
+@pytest.mark.parametrize("w", [W.WORKLOADS["tiny"], MID, MID_WIDE_I, W.WORKLOADS["decode"]],
+                         ids=["tiny", "mid", "mid_wide_i", "decode"])
 def test_layer_w8a8_parity(w):
     """moe_layer_forward_w8a8 against the oracle's W8A8 layer (near-tie rows for
     the selection the GPU made); repeated calls give the same bits."""
