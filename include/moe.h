@@ -288,9 +288,11 @@ moe_status moe_layer_forward_fp8(const moe_dims *d, const moe_bf16 *hidden, cons
  * quantised per row by the weight rule (E4M3, scale = max|row| / 448, codes
  * nearest-even of value / scale) from its own values at run time -- the hidden
  * state per token before the gate/up GEMM, and the bf16 SiLU(gate) * up
- * activation per routed slot (per token for the shared expert) as the down
- * GEMM loads it.  Each output element is (sum of code products) * row scale *
- * column scale, accumulated in fp32.  The router stays fp32.
+ * activation per routed slot (per token for the shared expert) once the
+ * gate/up GEMM has produced the whole row, before the down GEMM reads it (the
+ * codes and row scales are kept in the workspace).  Each output element is
+ * (sum of code products) * row scale * column scale, accumulated in fp32.  The
+ * router stays fp32.
  *   Shapes: H, I and I_shared multiples of 128 (else MOE_ERR_UNSUPPORTED).
  *   moe_expert_ffn_w8a8: arguments and results as for moe_expert_ffn_fp8; it
  *   first quantises `hidden` into the workspace, then runs the expert kernel.
