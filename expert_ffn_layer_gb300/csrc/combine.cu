@@ -27,9 +27,11 @@ __device__ __forceinline__ void acc8(float (&a)[8], const uint4 &v, float w) {
 }  // namespace
 
 // BATCHED: every slot's loads in flight at once (latency-bound small batches;
-// the register cost halves residency, which large, bandwidth-bound batches
-// need more), else one slot at a time.  Both add in slot order.
-template <bool BATCHED>
+// the register cost of top-16 halves residency, which large, bandwidth-bound
+// batches need more), else one slot at a time; K8: top-8 exactly, its eight
+// rows (and the shared one) in flight together with half that register cost.
+// All add in slot order.
+template <bool BATCHED, bool K8 = false>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
   pdl_wait();
   pdl_launch_dependents();
@@ -40,7 +42,21 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     const int t = (int)(idx / hv);
     const int c = (int)(idx - (long long)t * hv);
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if constexpr (!BATCHED) {
+    if constexpr (K8) {
+      uint4 v[8];
+      float wt[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int pos = min(max(__ldg(p.inv + (size_t)t * 8 + j), 0), p.S - 1);
+        wt[j] = __ldg(p.topk_w + (size_t)t * 8 + j);
+        v[j] = __ldcs(reinterpret_cast<const uint4 *>(p.y_sorted + (size_t)pos * p.H) + c);
+      }
+      uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      if (p.y_shared != nullptr) z = __ldcs(reinterpret_cast<const uint4 *>(p.y_shared + (size_t)t * p.H) + c);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc8(a, v[j], wt[j]);
+      if (p.y_shared != nullptr) acc8(a, z, 1.0f);
+    } else if constexpr (!BATCHED) {
       for (int j = 0; j < p.top_k; ++j) {
         const int pos = min(max(__ldg(p.inv + (size_t)t * p.top_k + j), 0), p.S - 1);
         const float w = __ldg(p.topk_w + (size_t)t * p.top_k + j);
@@ -97,8 +113,10 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream, bool pdl
   if (blocks < 1) blocks = 1;
   void *args[] = {(void *)&p};
   const bool batched = total <= (long long)nsm * kThreads;  // one wave of threads
-  return launch_ex(batched ? (const void *)combine_kernel<true> : (const void *)combine_kernel<false>,
-                   dim3((unsigned)blocks), dim3(kThreads), 0, stream, pdl, 1, args);
+  const void *fn = batched ? (const void *)combine_kernel<true>
+                   : p.top_k == 8 ? (const void *)combine_kernel<false, true>
+                                  : (const void *)combine_kernel<false>;
+  return launch_ex(fn, dim3((unsigned)blocks), dim3(kThreads), 0, stream, pdl, 1, args);
 }
 
 }  // namespace moe
