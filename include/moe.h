@@ -242,9 +242,8 @@ moe_status moe_fused_moe(const moe_dims *d, const moe_bf16 *hidden, const int32_
                          const moe_bf16 *ws_down, moe_bf16 *out, void *ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------ FP8
- * FP8 expert weights (next step of the survey's plan; [case] lists W8A8
- * quantised deployments and quantises inside the FusedMoE chain, but fixes no
- * format).  Reading: every expert matrix row (an output feature) is stored as
+ * FP8 expert weights ([case] lists W8A8 quantised deployments and quantises
+ * inside the FusedMoE chain, but fixes no format).  Reading: every expert matrix row (an output feature) is stored as
  * OCP E4M3 codes plus one fp32 scale, scale = max|row| / 448 (1 for a zero
  * row), code = E4M3 round-to-nearest-even of w / scale, saturated at 448.  The
  * layer uses value(code) * scale as the weight: the expert kernel feeds the
