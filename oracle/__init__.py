@@ -44,6 +44,11 @@ Readings where the pages are silent (each also listed in the design notes):
   matrix feeding an expert GEMM is quantised per row by the same rule, from its
   own values -- the hidden state per token, the bf16 SiLU(gate) * up activation
   per routed slot; the router stays fp32.
+* MXFP8 / MXFP4 (the Ascend deployment article, section 8.2, names them and
+  no more): the OCP Microscaling formats, blocks of 32 along the reduction axis
+  with a power-of-two scale 2^(floor(log2 max) - emax), E4M3 or E2M1 elements
+  nearest-even and saturated (``oracle/mx.py``; the article's hybrid: MXFP4
+  routed weights, MXFP8 shared weights and activations).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 against closed forms, hand-worked examples (``tests/golden/``), brute force on
